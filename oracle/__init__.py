@@ -1,0 +1,140 @@
+"""CPU oracle for NF4 weight-only quantization (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package imports nothing from it: the two share no code, header, table or
+constant.
+
+The arithmetic lives in ``nf4_oracle.c`` (plain C, compiled with gcc, no fast
+math, no FMA contraction).  This module compiles it on first use, loads it
+with ctypes and marshals numpy arrays.  Every function here is a thin call;
+the definitions, and the readings of the diffuseR page "Gemma3 NF4 on GPU"
+(pull request #39, Summary) they follow, are documented in the C file.
+
+All bf16 data crosses this interface as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nf4_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``nf4_oracle.c`` into ``liboracle.so`` beside it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I32 = ctypes.c_int32
+        lib.oracle_codebook.restype = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_codebook.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_nearest_code.argtypes = [P, I64, P]
+        lib.oracle_quantize.argtypes = [P, I64, I32, P, P]
+        lib.oracle_dequantize.argtypes = [P, P, I64, I32, P]
+        lib.oracle_linear.argtypes = [P, I64, I64, P, P, I64, I32, P]
+        for f in (lib.oracle_nearest_code, lib.oracle_quantize,
+                  lib.oracle_dequantize, lib.oracle_linear, lib.oracle_set_num_threads):
+            f.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+BLOCK = 64
+
+
+def codebook() -> np.ndarray:
+    """The oracle's 16 fp32 codebook values, ascending."""
+    lib = _load()
+    return np.ctypeslib.as_array(lib.oracle_codebook(), shape=(16,)).copy()
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def f32_to_bf16_bits(v: float) -> int:
+    return int(_load().oracle_f32_to_bf16(ctypes.c_float(v)))
+
+
+def nearest_code(n: np.ndarray) -> np.ndarray:
+    """Code chosen for each normalised fp32 value ``n``."""
+    n = np.ascontiguousarray(n, dtype=np.float32).ravel()
+    out = np.empty(n.size, dtype=np.uint8)
+    _load().oracle_nearest_code(_ptr(n), n.size, _ptr(out))
+    return out
+
+
+def quantize(w_bits: np.ndarray, block: int = BLOCK):
+    """bf16 bits (any shape, even size) -> (packed uint8 [numel/2], absmax fp32 [ceil(numel/block)])."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16).ravel()
+    if w.size % 2:
+        raise ValueError("numel must be even")
+    packed = np.empty(w.size // 2, dtype=np.uint8)
+    absmax = np.empty((w.size + block - 1) // block, dtype=np.float32)
+    _load().oracle_quantize(_ptr(w), w.size, block, _ptr(packed), _ptr(absmax))
+    return packed, absmax
+
+
+def dequantize(packed: np.ndarray, absmax: np.ndarray, numel: int, block: int = BLOCK) -> np.ndarray:
+    """(packed, absmax) -> bf16 bits [numel] by nibble unpack."""
+    p = np.ascontiguousarray(packed, dtype=np.uint8).ravel()
+    a = np.ascontiguousarray(absmax, dtype=np.float32).ravel()
+    if p.size * 2 < numel or a.size * block < numel:
+        raise ValueError("packed/absmax too small for numel")
+    out = np.empty(numel, dtype=np.uint16)
+    _load().oracle_dequantize(_ptr(p), _ptr(a), numel, block, _ptr(out))
+    return out
+
+
+def linear(x_bits: np.ndarray, packed: np.ndarray, absmax: np.ndarray, n_out: int,
+           block: int = BLOCK) -> np.ndarray:
+    """Y = X . deq(W)^T in fp64.  X is bf16 bits [M, K]; W is NF4 over [n_out, K]."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D")
+    M, K = x.shape
+    p = np.ascontiguousarray(packed, dtype=np.uint8).ravel()
+    a = np.ascontiguousarray(absmax, dtype=np.float32).ravel()
+    if p.size * 2 != n_out * K or a.size != (n_out * K + block - 1) // block:
+        raise ValueError("packed/absmax do not match [n_out, K]")
+    y = np.empty((M, n_out), dtype=np.float64)
+    _load().oracle_linear(_ptr(x), M, K, _ptr(p), _ptr(a), n_out, block, _ptr(y))
+    return y

@@ -1,0 +1,193 @@
+/*
+ * nf4_oracle.c -- plain CPU oracle for NF4 weight-only quantization.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes
+ * or calls this file.  It may be used by the tests, by the smoke check and by
+ * the benchmark's CPU-baseline leg, and by nothing else.  It shares no code,
+ * header, table or constant with the CUDA library: the codebook below is typed
+ * here a second time on purpose.
+ *
+ * What it computes (the source page is the diffuseR pull request "Gemma3 NF4
+ * on GPU: quantized encoder, batch encoding, byte-LUT eager dequant", #39,
+ * Summary paragraph): the seven projection weights of every Gemma3 layer are
+ * packed to NF4 while activations stay at the compute dtype (bf16), and the
+ * eager forward dequantizes them and runs a dense matmul.  The page prints
+ * neither the codebook, the block size, the scale dtype nor the nibble order.
+ * The readings used here:
+ *
+ *   - codebook: the 16-value NormalFloat-4 table of QLoRA (Dettmers et al.
+ *     2023, arXiv:2305.14314, appendix), stored as fp32 constants;
+ *   - blocks of 64 consecutive elements of the row-major flattened weight,
+ *     one fp32 absmax per block, no double quantization; a partial last block
+ *     uses the elements it has;
+ *   - code = the codebook index nearest to w / absmax (fp32 IEEE division),
+ *     distances compared in fp64, ties to the lower index; an all-zero block
+ *     gets absmax +0 and code 7 (value 0) everywhere;
+ *   - packing: element 2j in the high nibble of byte j, element 2j+1 in the
+ *     low nibble;
+ *   - dequant by nibble unpack (not a lookup table):
+ *     y = bf16_rne( float(bf16_rne(C[code])) * absmax ), one fp32 multiply;
+ *   - linear: Y[m][n] = sum_k X[m][k] * Wdeq[n][k], accumulated in fp64.
+ *
+ * Every loop below is the definition written out, one element at a time.
+ * OpenMP splits only the outermost independent loop (blocks or rows); it
+ * changes no arithmetic and no summation order.
+ *
+ * Parity pins for every exported function live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* NormalFloat-4 codebook, QLoRA appendix, ascending. */
+static const float ORACLE_NF4[16] = {
+    -1.0f,
+    -0.6961928009986877f,
+    -0.5250730514526367f,
+    -0.39491748809814453f,
+    -0.28444138169288635f,
+    -0.18477343022823334f,
+    -0.09105003625154495f,
+    0.0f,
+    0.07958029955625534f,
+    0.16093020141124725f,
+    0.24611230194568634f,
+    0.33791524171829224f,
+    0.44070982933044434f,
+    0.5626170039176941f,
+    0.7229568362236023f,
+    1.0f,
+};
+
+/* ---- bf16 <-> fp32 from the IEEE bit layout ----------------------------- */
+
+/* A bf16 value is the upper 16 bits of the fp32 with the same value. */
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round an fp32 to the nearest bf16, ties to even.  NaN maps to a quiet NaN
+ * with the sign kept.  Overflow rounds to infinity as IEEE prescribes. */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xffffu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* ---- exported ----------------------------------------------------------- */
+
+const float* oracle_codebook(void) { return ORACLE_NF4; }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+
+/* Index of the codebook value nearest to n; fp64 distances, the first
+ * (lowest) index wins a tie. */
+static int nearest_code(float n) {
+    int best = 0;
+    double best_d = fabs((double)n - (double)ORACLE_NF4[0]);
+    for (int k = 1; k < 16; ++k) {
+        double d = fabs((double)n - (double)ORACLE_NF4[k]);
+        if (d < best_d) {
+            best_d = d;
+            best = k;
+        }
+    }
+    return best;
+}
+
+/* Code selection alone, exposed so that the tests can sweep normalised
+ * values directly. */
+void oracle_nearest_code(const float* n, int64_t count, uint8_t* code) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i) code[i] = (uint8_t)nearest_code(n[i]);
+}
+
+/* Blockwise absmax quantization of a bf16 tensor of `numel` elements
+ * (numel even) into numel/2 packed bytes and ceil(numel/block) fp32 scales. */
+void oracle_quantize(const uint16_t* w, int64_t numel, int32_t block, uint8_t* packed,
+                     float* absmax) {
+    int64_t nblocks = (numel + block - 1) / block;
+    uint8_t* codes = (uint8_t*)malloc((size_t)numel);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblocks; ++b) {
+        int64_t lo = b * block;
+        int64_t hi = lo + block < numel ? lo + block : numel;
+        float am = 0.0f;
+        for (int64_t i = lo; i < hi; ++i) {
+            float a = fabsf(bf16_to_f32(w[i]));
+            if (a > am) am = a;
+        }
+        absmax[b] = am;
+        for (int64_t i = lo; i < hi; ++i) {
+            if (am == 0.0f) {
+                codes[i] = 7;
+            } else {
+                float n = bf16_to_f32(w[i]) / am;
+                codes[i] = (uint8_t)nearest_code(n);
+            }
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < numel / 2; ++j)
+        packed[j] = (uint8_t)((codes[2 * j] << 4) | codes[2 * j + 1]);
+    free(codes);
+}
+
+/* Dequantize by unpacking each nibble and scaling its bf16 codebook value. */
+void oracle_dequantize(const uint8_t* packed, const float* absmax, int64_t numel, int32_t block,
+                       uint16_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < numel; ++i) {
+        uint8_t byte = packed[i / 2];
+        int code = (i % 2 == 0) ? (byte >> 4) : (byte & 0x0f);
+        float c = bf16_to_f32(f32_to_bf16_rne(ORACLE_NF4[code]));
+        float y = c * absmax[i / block];
+        out[i] = f32_to_bf16_rne(y);
+    }
+}
+
+/* Y[M][N] = X[M][K] . Wdeq[N][K]^T in fp64, W given as NF4 (packed, absmax)
+ * over the flattened [N][K] weight.  X is bf16 bits, row-major. */
+void oracle_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                   const float* absmax, int64_t N, int32_t block, double* y) {
+    uint16_t* wq = (uint16_t*)malloc((size_t)(N * K) * sizeof(uint16_t));
+    oracle_dequantize(packed, absmax, N * K, block, wq);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)bf16_to_f32(x[m * K + k]) * (double)bf16_to_f32(wq[n * K + k]);
+            y[m * N + n] = acc;
+        }
+    }
+    free(wq);
+}
