@@ -1,0 +1,151 @@
+/*
+ * nf4.h -- C ABI of libnf4, an NF4 weight-only quantized linear layer for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation comes from the diffuseR pull request "Gemma3 NF4 on GPU:
+ * quantized encoder, batch encoding, byte-LUT eager dequant" (#39), Summary
+ * paragraph: the seven projection weights of each Gemma3-12B layer are packed
+ * to NF4 while activations stay at the compute dtype; the forward dequantizes
+ * through a byte lookup table straight into the output buffer and runs a
+ * dense matmul.  The page does not print the format; this library fixes it:
+ *
+ *   - codebook: the 16 NormalFloat-4 values of QLoRA (arXiv:2305.14314,
+ *     appendix), ascending, code 7 = 0.0;
+ *   - blocks of `block` = 64 consecutive elements of the row-major flattened
+ *     weight; one fp32 absmax per block (max |w| over the block), no double
+ *     quantization; a partial last block covers the elements it has;
+ *   - code = index of the codebook value nearest to w / absmax (fp32 IEEE
+ *     division), ties to the lower index; an all-zero block has absmax +0.0
+ *     and code 7 everywhere;
+ *   - packed byte j holds element 2j in its high nibble and element 2j+1 in
+ *     its low nibble;
+ *   - dequantized value = bf16_rne( float(bf16_rne(C[code])) * absmax ).
+ *
+ * bf16 tensors cross this interface as uint16_t bit patterns.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller (allocate
+ *     them however you like; the library never frees them).  The library
+ *     itself allocates nothing per call: it keeps, per device, one 4-byte
+ *     error word and cached kernel attributes, released when the process
+ *     exits.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is stream-ordered and asynchronous: it validates its
+ *     arguments on the host, enqueues its kernels and returns.  Nothing
+ *     synchronizes except nf4_last_error().
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned as a status; nothing runs on bad input.  A failed launch
+ *     returns NF4_ERR_CUDA.  A kernel whose internal wait exceeds its time
+ *     limit (about one second) records NF4_ERR_TIMEOUT in the device error word
+ *     and exits early; nf4_last_error() reports it.  No call aborts the
+ *     process or throws.
+ *   - The current CUDA device must be an sm_103 GPU (else NF4_ERR_DEVICE).
+ */
+#ifndef NF4_H_
+#define NF4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NF4_API __attribute__((visibility("default")))
+#else
+#define NF4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nf4_status {
+    NF4_OK = 0,
+    NF4_ERR_NULL = 1,       /* a required pointer is NULL */
+    NF4_ERR_SHAPE = 2,      /* a size is negative, odd where it must be even, or K % 64 != 0 */
+    NF4_ERR_ALIGN = 3,      /* a pointer lacks the alignment the entry point requires */
+    NF4_ERR_BLOCKSIZE = 4,  /* block != 64 */
+    NF4_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than nf4_linear_workspace_size() */
+    NF4_ERR_DEVICE = 6,     /* no current device, or it is not sm_103 */
+    NF4_ERR_CUDA = 7,       /* a CUDA runtime call or launch failed */
+    NF4_ERR_TIMEOUT = 8     /* a kernel gave up on a bounded wait (reported by nf4_last_error) */
+} nf4_status;
+
+/* The only block size supported. */
+#define NF4_BLOCK 64
+
+/*
+ * nf4_quantize -- blockwise absmax NF4 quantization of one bf16 tensor.
+ * Page: "Gemma3 NF4 on GPU" (#39), Summary: projection weights "pack to NF4".
+ *
+ *   w       [numel] bf16 bits, any layout the caller flattens row-major
+ *   numel   number of elements; even, >= 0 (0 enqueues nothing)
+ *   block   must be NF4_BLOCK
+ *   packed  [numel / 2] bytes out
+ *   absmax  [ceil(numel / 64)] fp32 out
+ *
+ * Alignment: none required; 16-byte aligned w and 4-byte aligned packed take
+ * the vectorized kernel, anything else a slower element-wise kernel with
+ * identical results.  Results are bit-exact: one correct answer exists.
+ * Inputs must be finite (NaN/Inf give unspecified codes).
+ */
+NF4_API nf4_status nf4_quantize(const uint16_t* w, int64_t numel, int32_t block, uint8_t* packed,
+                        float* absmax, void* stream);
+
+/*
+ * nf4_dequantize -- NF4 to bf16 through a 256-entry byte lookup table.
+ * Page: "Gemma3 NF4 on GPU" (#39), Summary: the eager dequant uses a byte LUT,
+ * one index per packed byte, gathered straight into the output buffer.
+ *
+ *   packed  [numel / 2] bytes;  absmax [ceil(numel / 64)] fp32
+ *   numel   even, >= 0;  block must be NF4_BLOCK
+ *   out     [numel] bf16 bits
+ *
+ * Alignment: none required; 16-byte aligned out and 4-byte aligned packed take
+ * the vectorized kernel.  Bit-exact.
+ */
+NF4_API nf4_status nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t numel,
+                          int32_t block, uint16_t* out, void* stream);
+
+/*
+ * nf4_linear -- Y = X . deq(W)^T, the NF4 weight-only linear layer (no bias).
+ * Page: "Gemma3 NF4 on GPU" (#39), Summary: ltx23_nf4_linear, the module the
+ * loader swaps in for each projection.
+ *
+ *   x        [M, K] bf16 bits, row-major (row pitch K)
+ *   packed   [N, K / 2] bytes and absmax [N, K / 64] fp32: W [N, K] quantized
+ *            by nf4_quantize (row-major flattening)
+ *   y        [M, N] bf16 bits out, row-major; fp32 accumulation, one bf16
+ *            rounding at the end
+ *   workspace, workspace_bytes  scratch of at least
+ *            nf4_linear_workspace_size(M, N, K) bytes (may be NULL when that
+ *            size is 0); contents need no initialisation and are clobbered
+ *
+ * Requirements: M, N >= 0, K > 0, K % 64 == 0, block == NF4_BLOCK; x, packed, y
+ * and workspace 16-byte aligned, absmax 4-byte aligned.  Not bit-exact: the
+ * fp32 accumulation order is the kernel's; the result matches an fp64 matmul of
+ * the dequantized weights to within bf16 output rounding plus fp32 summation
+ * error.  Rows of Y are independent of each other.
+ */
+NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                      const float* absmax, int64_t N, int32_t block, uint16_t* y,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace nf4_linear needs for this shape (host only, no device
+ * call).  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad arguments. */
+NF4_API nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/* Synchronize `stream`, then read and clear this device's error word.
+ * Returns NF4_OK, NF4_ERR_TIMEOUT (a kernel gave up on a wait), or
+ * NF4_ERR_CUDA if the synchronization itself failed. */
+NF4_API nf4_status nf4_last_error(void* stream);
+
+/* Static, NUL-terminated name of a status code ("NF4_OK", ...). */
+NF4_API const char* nf4_status_string(nf4_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+NF4_API int32_t nf4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4_H_ */

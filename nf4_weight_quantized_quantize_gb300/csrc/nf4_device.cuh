@@ -1,0 +1,313 @@
+// nf4_device.cuh -- device-side constants and PTX wrappers shared by the
+// libnf4 kernels (sm_103a only).
+//
+// Format (diffuseR pull request "Gemma3 NF4 on GPU" #39, Summary, with the
+// format fixed as documented in include/nf4.h): 16-value NF4 codebook,
+// 64-element blocks, fp32 absmax, element 2j in the high nibble of byte j.
+#pragma once
+
+#include <bit>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#ifndef NF4_WAIT_LIMIT_NS
+// A bounded wait gives up after this long (nanoseconds of %globaltimer).
+#define NF4_WAIT_LIMIT_NS 1000000000ull
+#endif
+
+namespace nf4 {
+
+constexpr int kBlock = 64;
+
+// NormalFloat-4 codebook of QLoRA (arXiv:2305.14314, appendix), ascending.
+constexpr float kCode[16] = {
+    -1.0f,
+    -0.6961928009986877f,
+    -0.5250730514526367f,
+    -0.39491748809814453f,
+    -0.28444138169288635f,
+    -0.18477343022823334f,
+    -0.09105003625154495f,
+    0.0f,
+    0.07958029955625534f,
+    0.16093020141124725f,
+    0.24611230194568634f,
+    0.33791524171829224f,
+    0.44070982933044434f,
+    0.5626170039176941f,
+    0.7229568362236023f,
+    1.0f,
+};
+
+// Decision threshold between codes j and j+1.  The exact midpoint
+// m = (C[j] + C[j+1]) / 2 is computed in fp64 (exact for two fp32 values).
+// If m is an fp32 value the threshold is m; otherwise it is the largest fp32
+// below m.  For every fp32 n, n > threshold exactly when n > m, so
+// code(n) = #{ j : n > thr(j) } is the nearest codebook index with ties going
+// to the lower index.
+constexpr float threshold(int j) {
+    double m = (static_cast<double>(kCode[j]) + static_cast<double>(kCode[j + 1])) * 0.5;
+    float f = static_cast<float>(m);
+    if (static_cast<double>(f) > m) {
+        uint32_t u = std::bit_cast<uint32_t>(f);
+        u = (f > 0.0f) ? u - 1u : u + 1u;   // one step toward -inf
+        f = std::bit_cast<float>(u);
+    }
+    return f;
+}
+
+// Device copies (constant bank).  c_thr[15] = +inf pads the table to 16 so a
+// binary search can index it without a bound check.
+static __constant__ float c_code[16] = {
+    kCode[0], kCode[1], kCode[2],  kCode[3],  kCode[4],  kCode[5],  kCode[6],  kCode[7],
+    kCode[8], kCode[9], kCode[10], kCode[11], kCode[12], kCode[13], kCode[14], kCode[15],
+};
+static __constant__ float c_thr[16] = {
+    threshold(0),  threshold(1),  threshold(2),  threshold(3),  threshold(4),
+    threshold(5),  threshold(6),  threshold(7),  threshold(8),  threshold(9),
+    threshold(10), threshold(11), threshold(12), threshold(13), threshold(14),
+    __builtin_huge_valf(),
+};
+
+// Error word codes (first error wins; the host reports any nonzero word as a timeout).
+enum : uint32_t {
+    kErrTimeoutFull = 0x101,      // waiting for a loaded stage
+    kErrTimeoutEmpty = 0x102,     // waiting for a stage to be released
+    kErrTimeoutConverted = 0x103, // waiting for converted weights
+    kErrTimeoutAccum = 0x104,     // waiting for the accumulator
+    kErrTimeoutDrain = 0x105,     // waiting for copies in flight at exit
+};
+
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- loads
+
+__device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ldg_nc_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- bf16 helpers
+
+// Two fp32 values -> one bf16x2 word (first in the low half), each rounded to
+// nearest even by the hardware conversion.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// A LUT entry for packed byte b: bf16(C[b >> 4]) in the low half (the element
+// at the lower address) and bf16(C[b & 15]) in the high half.
+__device__ __forceinline__ uint32_t lut_entry(uint32_t b) {
+    return pack_bf16x2(c_code[b >> 4], c_code[b & 15]);
+}
+
+// Scale one LUT entry by the block absmax: each bf16 widened to fp32, one
+// fp32 multiply, one rounding back to bf16.
+__device__ __forceinline__ uint32_t scale_entry(uint32_t e, float am) {
+    float lo = __uint_as_float(e << 16);
+    float hi = __uint_as_float(e & 0xffff0000u);
+    return pack_bf16x2(lo * am, hi * am);
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// NF4_WAIT_LIMIT_NS.  Gives up early when *abort becomes nonzero (another
+// role of this CTA gave up).  On giving up, records `code` in the device
+// error word, raises *abort and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort, uint32_t code) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+#pragma unroll 1
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > NF4_WAIT_LIMIT_NS) {
+            record_error(err, code);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 2-D tiled load of box {x, y} into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, both K-major bf16, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored with the
+// 128-byte swizzle: rows of 128 bytes (64 bf16), 8-row atoms 1024 bytes apart.
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29,
+// unused for swizzled K-major, set to 1), stride byte offset >> 4 (32-45),
+// fixed 0b001 (46-48), base offset 0 (49-51), swizzle mode 2 = 128B (61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: bf16 A and B, fp32 D, both K-major,
+// no negation or sparsity; N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)            // D format: f32
+           | (1u << 7)          // A format: bf16
+           | (1u << 10)         // B format: bf16
+           | (0u << 15)         // A K-major
+           | (0u << 16)         // B K-major
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+}  // namespace nf4

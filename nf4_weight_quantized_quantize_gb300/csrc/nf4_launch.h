@@ -1,0 +1,41 @@
+// nf4_launch.h -- internal interface between the C ABI front end
+// (nf4_capi.cu) and the kernel launchers.  Not installed, not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace nf4 {
+
+struct DeviceInfo {
+    int ordinal = -1;
+    int sm_count = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    size_t smem_optin = 0;     // max dynamic shared memory per block (opt-in)
+    uint32_t* err_word = nullptr;  // device address of this device's error word
+};
+
+cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t numel, uint8_t* packed,
+                            float* absmax, cudaStream_t s);
+
+cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, const float* absmax,
+                              int64_t numel, uint16_t* out, cudaStream_t s);
+
+// Fused NF4 GEMM, M >= 128 path (tcgen05 / TMEM).
+cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
+                        cudaStream_t s);
+
+// Workspace bytes the skinny (M < 128) path needs for this shape.
+size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K);
+
+// Skinny path: swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an
+// ordered reduction.
+cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+                          const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
+                          void* workspace, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace nf4

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/nf4.h declares, and rejects bad arguments on the host before touching
+a device (the "hard error, never run on garbage" convention of the diffuseR
+page "Gemma3 NF4 on GPU", #39, Summary: the loader hard-errors on unfilled
+parameters)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nf4_weight_quantized_quantize_gb300 as nf4
+from nf4_weight_quantized_quantize_gb300 import build as nf4_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nf4_build.build()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^NF4_API\s+[\w\s\*]+?\b(nf4_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"nf4_quantize", "nf4_dequantize", "nf4_linear", "nf4_linear_workspace_size",
+            "nf4_last_error", "nf4_status_string", "nf4_version"} <= set(names)
+    lib = ctypes.CDLL(nf4.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_links_no_torch_and_no_libcuda():
+    import subprocess
+    out = subprocess.run(["ldd", nf4.LIB_PATH], capture_output=True, text=True).stdout
+    assert "torch" not in out and "libcuda.so" not in out and "libcudart" not in out
+
+
+def test_status_strings_and_version():
+    for code, name in [(0, "NF4_OK"), (1, "NF4_ERR_NULL"), (2, "NF4_ERR_SHAPE"), (3, "NF4_ERR_ALIGN"),
+                       (4, "NF4_ERR_BLOCKSIZE"), (5, "NF4_ERR_WORKSPACE"), (6, "NF4_ERR_DEVICE"),
+                       (7, "NF4_ERR_CUDA"), (8, "NF4_ERR_TIMEOUT")]:
+        assert nf4.nf4_status_string(code) == name
+    assert nf4.nf4_status_string(99) == "NF4_ERR_UNKNOWN"
+    assert nf4.nf4_version() >= 100
+
+
+FAKE = 1 << 20   # a 16-byte aligned non-null address; never dereferenced by these calls
+
+
+def test_quantize_argument_errors():
+    assert nf4.nf4_quantize(FAKE, 128, 32, FAKE, FAKE) == nf4.NF4_ERR_BLOCKSIZE
+    assert nf4.nf4_quantize(FAKE, 127, 64, FAKE, FAKE) == nf4.NF4_ERR_SHAPE
+    assert nf4.nf4_quantize(FAKE, -2, 64, FAKE, FAKE) == nf4.NF4_ERR_SHAPE
+    assert nf4.nf4_quantize(0, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_quantize(FAKE, 128, 64, 0, FAKE) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_quantize(FAKE, 128, 64, FAKE, 0) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_quantize(FAKE + 1, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_quantize(FAKE, 128, 64, FAKE, FAKE + 2) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_quantize(0, 0, 64, 0, 0) == nf4.NF4_OK       # empty: nothing to do
+
+
+def test_dequantize_argument_errors():
+    assert nf4.nf4_dequantize(FAKE, FAKE, 128, 128, FAKE) == nf4.NF4_ERR_BLOCKSIZE
+    assert nf4.nf4_dequantize(FAKE, FAKE, 3, 64, FAKE) == nf4.NF4_ERR_SHAPE
+    assert nf4.nf4_dequantize(0, FAKE, 128, 64, FAKE) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_dequantize(FAKE, 0, 128, 64, FAKE) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_dequantize(FAKE, FAKE, 128, 64, 0) == nf4.NF4_ERR_NULL
+    assert nf4.nf4_dequantize(FAKE, FAKE, 128, 64, FAKE + 1) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_dequantize(0, 0, 0, 64, 0) == nf4.NF4_OK
+
+
+def test_linear_argument_errors():
+    ok = dict(x=FAKE, M=256, K=128, packed=FAKE, absmax=FAKE, N=64, block=64, y=FAKE,
+              workspace=0, workspace_bytes=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return nf4.nf4_linear(a["x"], a["M"], a["K"], a["packed"], a["absmax"], a["N"], a["block"],
+                              a["y"], a["workspace"], a["workspace_bytes"])
+
+    assert call(block=128) == nf4.NF4_ERR_BLOCKSIZE
+    assert call(K=96) == nf4.NF4_ERR_SHAPE
+    assert call(K=0) == nf4.NF4_ERR_SHAPE
+    assert call(M=-1) == nf4.NF4_ERR_SHAPE
+    assert call(N=-5) == nf4.NF4_ERR_SHAPE
+    assert call(M=1 << 31) == nf4.NF4_ERR_SHAPE
+    assert call(x=0) == nf4.NF4_ERR_NULL
+    assert call(packed=0) == nf4.NF4_ERR_NULL
+    assert call(absmax=0) == nf4.NF4_ERR_NULL
+    assert call(y=0) == nf4.NF4_ERR_NULL
+    assert call(x=FAKE + 2) == nf4.NF4_ERR_ALIGN
+    assert call(packed=FAKE + 8) == nf4.NF4_ERR_ALIGN
+    assert call(y=FAKE + 4) == nf4.NF4_ERR_ALIGN
+    assert call(absmax=FAKE + 2) == nf4.NF4_ERR_ALIGN
+    assert call(M=0) == nf4.NF4_OK and call(N=0) == nf4.NF4_OK
+    st, need = nf4.nf4_linear_workspace_size(16, 3840, 15360)
+    assert st == nf4.NF4_OK
+    if need:
+        assert call(M=16, N=3840, K=15360) == nf4.NF4_ERR_WORKSPACE
+        assert call(M=16, N=3840, K=15360, workspace=FAKE, workspace_bytes=need - 1) == nf4.NF4_ERR_WORKSPACE
+        assert call(M=16, N=3840, K=15360, workspace=FAKE + 4, workspace_bytes=need) == nf4.NF4_ERR_ALIGN
+
+
+def test_workspace_size_rules():
+    assert nf4.nf4_linear_workspace_size(2048, 4096, 3840) == (nf4.NF4_OK, 0)
+    assert nf4.nf4_linear_workspace_size(16, 4096, 100)[0] == nf4.NF4_ERR_SHAPE
+    assert nf4.nf4_linear_workspace_size(-1, 4096, 128)[0] == nf4.NF4_ERR_SHAPE
+    st, b = nf4.nf4_linear_workspace_size(0, 4096, 128)
+    assert st == nf4.NF4_OK and b == 0
+    assert nf4.lib().nf4_linear_workspace_size(16, 16, 64, None) == nf4.NF4_ERR_NULL
+
+
+def test_no_device_is_reported_not_crashed():
+    """With arguments that pass validation and no usable GPU the call returns
+    NF4_ERR_DEVICE (on a GPU machine this test is skipped)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert nf4.nf4_quantize(FAKE, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_DEVICE
+    assert nf4.nf4_last_error(0) == nf4.NF4_ERR_DEVICE
