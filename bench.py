@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the NF4 weight-only linear hot path on one GB300 (or N replicas).
+
+One step is one pass of the whole path over one batch of synthetic input on
+the Gemma3-12B q_proj shape (W [4096, 3840] bf16 ~ N(0, 0.02), X [2048, 3840]
+bf16 ~ N(0, 1) = 2 prompts x 1024 tokens):
+
+    nf4_quantize(W) -> packed, absmax          blockwise absmax + nibble pack
+    nf4_dequantize(packed, absmax) -> Wdeq      byte-LUT dequant (bulk path)
+    nf4_linear(X, packed, absmax) -> Y          fused NF4 GEMM, M = 2048
+    nf4_linear(X[:16], packed, absmax) -> Ys    skinny path, M = 16
+
+`value` is the linear FLOPs of a step (2*M*N*K for both calls) divided by the
+step time, summed over ranks (replicas, weak scaling).  Inputs are resident in
+HBM; an L2 flush (a 512 MiB memset, outside the events) precedes every step.
+Per-kernel times come from CUDA events around each call on the launching
+stream.  `e2e` repeats the step through the public API with W and X copied
+from pinned host memory and Y, Ys copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (the plain C reference this library
+is checked against) on a bounded sample of the same step: it is the baseline
+arm, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "nf4_linear TFLOP/s at M=2048 Gemma3-12B projections; dequant HBM GB/s vs peak"
+CFG = workloads.Q_PROJ
+SKINNY_M = 16
+FLOPS_PER_STEP = 2 * CFG.m * CFG.n * CFG.k + 2 * SKINNY_M * CFG.n * CFG.k
+# Algorithmic bytes per weight element: quantize reads 2 and writes 0.5 + 4/64;
+# dequantize reads 0.5 + 4/64 and writes 2.
+BYTES_PER_W_QUANT = 2.5625
+BYTES_PER_W_DEQUANT = 2.5625
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+CPU_SAMPLE_ROWS = 1024          # cpu_baseline: linear on this many of the 2048 rows
+REF_STEP_ROWS = 128             # reference arm: rows of X per step
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"])}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nf4_weight_quantized_quantize_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` on this workload from the committed ncu
+    summaries, if they were taken on the current kernel sources; else None."""
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    want = kernel_source_hash()
+    for fn in sorted(os.listdir(prof)):
+        if not fn.endswith(".md"):
+            continue
+        text = open(os.path.join(prof, fn)).read()
+        for m in re.finditer(r"^traffic\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=(\d+)\s+"
+                             r"source_hash=(\w+)", text, flags=re.M):
+            if m.group(1) == kernel and m.group(2) == CFG.name and m.group(4) == want:
+                return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read only) on a
+    background thread while the timed region runs."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples = []
+        self.max_mhz = None
+        self.error = None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.handle)) != 0:
+                raise RuntimeError(f"no NVML handle for {bus!r}")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception as e:  # noqa: BLE001 - clocks are reported as unavailable
+            self.error = str(e)
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rsn = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                    self._reasons_fn(self.handle, ctypes.byref(rsn)) == 0:
+                self.samples.append((clk.value, rsn.value))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.error is None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            if not self.samples:   # region shorter than one period: take one reading now
+                self._stop.clear()
+                clk, rsn = ctypes.c_uint(), ctypes.c_ulonglong()
+                if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                        self._reasons_fn(self.handle, ctypes.byref(rsn)) == 0:
+                    self.samples.append((clk.value, rsn.value))
+
+    def summary(self):
+        if self.error is not None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"nvml unavailable: {self.error}"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle")
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def allreduce_max(value: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: int, steps: int, step_ms_max: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each ran `steps` steps,
+    timed by the slowest rank."""
+    return world * flops_per_step * steps / (step_ms_max * 1e-3) / 1e12
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+
+
+def oracle_sample(rows: int, x_bits, w_bits):
+    """One bounded sample of the step on the CPU oracle; returns (flops, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    p, a = oracle.quantize(w_bits)
+    oracle.dequantize(p, a, w_bits.size)
+    oracle.linear(x_bits[:rows], p, a, CFG.n)
+    oracle.linear(x_bits[:SKINNY_M], p, a, CFG.n)
+    dt = time.perf_counter() - t0
+    return 2 * (rows + SKINNY_M) * CFG.n * CFG.k, dt
+
+
+def cpu_baseline(rows: int = CPU_SAMPLE_ROWS):
+    import oracle
+    w = workloads.bits(workloads.make_weight(CFG))
+    x = workloads.bits(workloads.make_activation(CFG))
+    flops, dt = oracle_sample(rows, x, w)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"quantize + dequantize of the full W [{CFG.n}, {CFG.k}], linear on {rows} of the "
+                       f"{CFG.m} rows of X plus the {SKINNY_M}-row skinny batch; fp64 accumulation; "
+                       f"{dt:.2f} s")}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = workloads.bits(workloads.make_weight(CFG))
+    x = workloads.bits(workloads.make_activation(CFG))
+    for _ in range(args.warmup):
+        oracle_sample(REF_STEP_ROWS, x, w)
+    total_flops, total_s = 0, 0.0
+    for _ in range(args.steps):
+        f, dt = oracle_sample(REF_STEP_ROWS, x, w)
+        total_flops += f
+        total_s += dt
+    value = total_flops / total_s / 1e12
+    sample = (f"per step: quantize + dequantize of the full W [{CFG.n}, {CFG.k}], linear on "
+              f"{REF_STEP_ROWS} of the {CFG.m} rows of X plus the {SKINNY_M}-row batch")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_block(args):
+    return {"workload": CFG.name, "M": CFG.m, "N": CFG.n, "K": CFG.k, "skinny_M": SKINNY_M,
+            "block": 64, "absmax": "fp32", "w_dist": "N(0,0.02) bf16", "x_dist": "N(0,1) bf16",
+            "seeds": {"w": CFG.w_seed, "x": CFG.x_seed}, "l2": "flushed before every step (512 MiB memset)",
+            "parallelism": f"replicas{args.gpus}"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import nf4_weight_quantized_quantize_gb300 as nf4
+
+    stream = torch.cuda.current_stream(dev)
+    w = workloads.make_weight(CFG, device=dev)
+    x = workloads.make_activation(CFG, device=dev)
+    xs = x[:SKINNY_M].contiguous()
+    numel = w.numel()
+    packed = torch.empty(numel // 2, dtype=torch.uint8, device=dev)
+    absmax = torch.empty(numel // 64, dtype=torch.float32, device=dev)
+    wdeq = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(CFG.m, CFG.n, dtype=torch.bfloat16, device=dev)
+    ys = torch.empty(SKINNY_M, CFG.n, dtype=torch.bfloat16, device=dev)
+    st, ws_bytes = nf4.nf4_linear_workspace_size(SKINNY_M, CFG.n, CFG.k)
+    assert st == nf4.NF4_OK
+    wsp = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    names = ["nf4_quantize", "nf4_dequantize", "nf4_linear_m2048", "nf4_linear_m16"]
+    calls = [
+        lambda: nf4.quantize(w, out=(packed, absmax)),
+        lambda: nf4.dequantize(packed, absmax, numel, out=wdeq),
+        lambda: nf4.linear(x, packed, absmax, CFG.n, out=y),
+        lambda: nf4.linear(xs, packed, absmax, CFG.n, out=ys, workspace=wsp),
+    ]
+
+    def step(evs=None):
+        for i, c in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            c()
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
+        raise RuntimeError("a kernel reported a timeout during warm-up")
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [(mk(), mk()) for _ in range(args.steps)]
+    call_ev = [[(mk(), mk()) for _ in calls] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    launches0 = nf4.nf4_launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step_ev[k][0].record(stream)
+        step(call_ev[k])
+        step_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(ws)
+    sampler.stop()
+    launches = nf4.nf4_launch_count() - launches0
+    if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
+        raise RuntimeError("a kernel reported a timeout in the timed region")
+
+    step_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    per_call = [statistics.mean(call_ev[k][i][0].elapsed_time(call_ev[k][i][1]) for k in range(args.steps))
+                for i in range(len(calls))]
+    step_ms = allreduce_max(step_ms, ws, dev)
+    value = aggregate_tflops(FLOPS_PER_STEP, args.steps, step_ms, ws)
+
+    # ---- end to end through the public API, host buffers
+    w_h = w.cpu().pin_memory()
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty(CFG.m, CFG.n, dtype=torch.bfloat16).pin_memory()
+    ys_h = torch.empty(SKINNY_M, CFG.n, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        w.copy_(w_h, non_blocking=True)
+        x.copy_(x_h, non_blocking=True)
+        xs.copy_(x[:SKINNY_M])
+        step()
+        y_h.copy_(y, non_blocking=True)
+        ys_h.copy_(ys, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    e2e_ev = [(mk(), mk()) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        e2e_step()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = allreduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), ws, dev)
+    e2e_value = aggregate_tflops(FLOPS_PER_STEP, args.steps, e2e_ms, ws)
+    h2d = (w.numel() + x.numel()) * 2
+    d2h = (y.numel() + ys.numel()) * 2
+
+    if rank != 0:
+        return 0
+    pk, pk_kind = peaks()
+    t_q, t_d, t_l, t_s = per_call
+    lin_tflops = 2 * CFG.m * CFG.n * CFG.k / (t_l * 1e-3) / 1e12
+    deq_gbs = numel * BYTES_PER_W_DEQUANT / (t_d * 1e-3) / 1e9
+    q_gbs = numel * BYTES_PER_W_QUANT / (t_q * 1e-3) / 1e9
+    sk_bytes = numel * 0.5625 + 2 * SKINNY_M * CFG.k + 2 * SKINNY_M * CFG.n
+    sk_gbs = sk_bytes / (t_s * 1e-3) / 1e9
+    clocks = sampler.summary()
+    traffic = profiled_traffic("gemm_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(args),
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (nf4_linear, M=2048)",
+                     "achieved": lin_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": lin_tflops / pk["bf16_tflops"], "peak_source": f"bf16_tflops of {pk_kind}",
+                     "traffic": traffic, "algorithmic": "2*M*N*K FLOP per launch"},
+        "kernels": {
+            "nf4_quantize": {"ms": t_q, "GB/s": q_gbs, "frac_hbm": q_gbs / pk["hbm_gbs"],
+                             "bytes_per_weight": BYTES_PER_W_QUANT},
+            "nf4_dequantize": {"ms": t_d, "GB/s": deq_gbs, "frac_hbm": deq_gbs / pk["hbm_gbs"],
+                               "bytes_per_weight": BYTES_PER_W_DEQUANT},
+            "nf4_linear_m2048": {"ms": t_l, "TFLOP/s": lin_tflops, "frac_bf16": lin_tflops / pk["bf16_tflops"]},
+            "nf4_linear_m16": {"ms": t_s, "GB/s": sk_gbs, "frac_hbm": sk_gbs / pk["hbm_gbs"],
+                               "bytes": sk_bytes},
+        },
+        "peaks": {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"], "source": pk_kind},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="omit the CPU oracle timing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

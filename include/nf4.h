@@ -144,6 +144,10 @@ NF4_API const char* nf4_status_string(nf4_status status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 NF4_API int32_t nf4_version(void);
 
+/* Number of kernels this library has enqueued in this process, on any
+ * device or stream (a monotone counter, for accounting and tests). */
+NF4_API uint64_t nf4_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

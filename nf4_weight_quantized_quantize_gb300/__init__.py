@@ -51,12 +51,14 @@ def _load():
         "nf4_last_error": [P],
         "nf4_status_string": [ctypes.c_int],
         "nf4_version": [],
+        "nf4_launch_count": [],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = ctypes.c_int
     lib.nf4_status_string.restype = ctypes.c_char_p
+    lib.nf4_launch_count.restype = ctypes.c_uint64
     return lib
 
 
@@ -110,6 +112,10 @@ def nf4_status_string(status: int) -> str:
 
 def nf4_version() -> int:
     return lib().nf4_version()
+
+
+def nf4_launch_count() -> int:
+    return lib().nf4_launch_count()
 
 
 # ---------------------------------------------------------------- torch tensors

@@ -52,8 +52,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, extra: list[str]) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], build_dir: str) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -61,28 +61,39 @@ def _compile(src: str, extra: list[str]) -> tuple[str, str]:
     return obj, r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile csrc/*.cu into libnf4.so (skipped when up to date)."""
-    if not force and not extra and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          out: str | None = None) -> str:
+    """Compile csrc/*.cu into libnf4.so (skipped when up to date).
+
+    `extra` adds nvcc flags (e.g. -D test switches) and then `out` must name a
+    different library path, so the product library is never built with them."""
+    lib = out or LIB
+    if extra and lib == LIB:
+        raise ValueError("a build with extra flags needs its own output path")
+    if not force and lib == LIB and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and lib != LIB and os.path.exists(lib) and \
+            all(os.path.getmtime(d) <= os.path.getmtime(lib) for d in _deps()):
+        return lib
+    build_dir = BUILD if lib == LIB else os.path.join(BUILD, os.path.basename(lib) + ".d")
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra or []), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra or [], build_dir), srcs))
     if verbose:
         for obj, log in results:
             print(f"== {os.path.basename(obj)}\n{log}")
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results],
            "-ldl", "-lrt", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         for obj, log in results:
             f.write(f"== {os.path.basename(obj)}\n{log}\n")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -4,6 +4,7 @@
 // the caller's stream.  Per device it keeps the device properties and the
 // address of a 4-byte error word that kernels set when a bounded wait gives
 // up.  Nothing here allocates device memory.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/nf4.h"
@@ -66,7 +67,11 @@ nf4_status current_device(const nf4::DeviceInfo** out) {
 
 inline bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+std::atomic<uint64_t> g_launches{0};
+
 }  // namespace
+
+void nf4::count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 extern "C" {
 
@@ -161,5 +166,7 @@ const char* nf4_status_string(nf4_status status) {
 }
 
 int32_t nf4_version(void) { return 100; }
+
+uint64_t nf4_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -69,6 +69,20 @@ __device__ __forceinline__ void convert_row(const uint8_t* prow, uint8_t* brow, 
     }
 }
 
+// Whether a converter warp reports K-slice kb as converted.  Always true in
+// the library.  A test build (-DNF4_TEST_DROP_CONVERTED_ARRIVE) withholds the
+// report for slice 0 -- a flag that nothing sets -- so the MMA issuer's bounded
+// wait runs out and the timeout path (error word, drain, TMEM release, early
+// exit) can be checked on a GPU without faulting or hanging it.
+__device__ __forceinline__ bool report_converted(int kb) {
+#ifdef NF4_TEST_DROP_CONVERTED_ARRIVE
+    return kb != 0;
+#else
+    (void)kb;
+    return true;
+#endif
+}
+
 // Wait (bounded) for the copies a producer issued into the last `stages`
 // K-slices to land, so no TMA write targets shared memory after exit.
 __device__ __forceinline__ void drain_tma(const Barriers& bar, int issued, int stages,
@@ -229,7 +243,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             convert_row(p_tile(s) + r * kPackedRow, b_tile(s) + r * 128, r, lut, am);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar.conv(s));
+            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(s));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
@@ -435,7 +449,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             convert_row(p_tile(s) + r * kPackedRow, a_tile(s) + r * 128, r, lut, am);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar.conv(s));
+            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(s));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
@@ -550,6 +564,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int
     const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
     gemm_kernel<<<static_cast<unsigned>(tiles), THREADS, SMEM, s>>>(tm_x, tm_w, a);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -566,6 +581,7 @@ static cudaError_t launch_skinny_t(const DeviceInfo& dev, const SkinnyPlan& p, c
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(skinny_kernel<MPAD>), smem, dev.ordinal); e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(p.splits));
     skinny_kernel<MPAD><<<grid, skinny::THREADS, smem, s>>>(tm_x, tm_w, a);
+    count_launches(1);
     return cudaGetLastError();
 }
 
@@ -589,6 +605,7 @@ cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, i
         case 80: e = launch_skinny_t<80>(dev, p, tm_x, tm_w, a, s); break;
         case 96: e = launch_skinny_t<96>(dev, p, tm_x, tm_w, a, s); break;
         case 112: e = launch_skinny_t<112>(dev, p, tm_x, tm_w, a, s); break;
+        case 128: e = launch_skinny_t<128>(dev, p, tm_x, tm_w, a, s); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
@@ -596,6 +613,7 @@ cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, i
     const int threads = 256;
     const int grid = static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
     splitk_reduce_kernel<<<grid, threads, 0, s>>>(static_cast<const float*>(workspace), p.splits, mn, y);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@ struct DeviceInfo {
     uint32_t* err_word = nullptr;  // device address of this device's error word
 };
 
+// Add n to the process-wide count of enqueued kernels (nf4_launch_count).
+void count_launches(int n);
+
 cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t numel, uint8_t* packed,
                             float* absmax, cudaStream_t s);
 

@@ -198,6 +198,7 @@ cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t nu
                                   kQuantThreads, (ntiles + kQuantThreads / 32 - 1) / (kQuantThreads / 32));
         quantize_vec_kernel<<<grid, kQuantThreads, 0, s>>>(reinterpret_cast<const uint4*>(w), nwords,
                                                           reinterpret_cast<uint32_t*>(packed), absmax);
+        count_launches(1);
         scalar_from = full;
     }
     if (scalar_from < nblocks) {
@@ -205,6 +206,7 @@ cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t nu
         const int threads = 128;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
         quantize_scalar_kernel<<<grid, threads, 0, s>>>(w, numel, scalar_from, nblocks, packed, absmax);
+        count_launches(1);
     }
     return cudaGetLastError();
 }
@@ -223,6 +225,7 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
                                       kDequantThreads, (ntiles + kDequantThreads / 32 - 1) / (kDequantThreads / 32));
             dequant_vec_kernel<<<grid, kDequantThreads, 0, s>>>(
                 reinterpret_cast<const uint32_t*>(packed), absmax, ntiles, reinterpret_cast<uint4*>(out));
+            count_launches(1);
         }
         scalar_from = ntiles * 512;
     }
@@ -231,6 +234,7 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
         const int threads = 256;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 8 * static_cast<int64_t>(dev.sm_count)));
         dequant_scalar_kernel<<<grid, threads, 0, s>>>(packed, absmax, scalar_from, nbytes, out);
+        count_launches(1);
     }
     return cudaGetLastError();
 }

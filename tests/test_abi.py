@@ -33,7 +33,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
     assert {"nf4_quantize", "nf4_dequantize", "nf4_linear", "nf4_linear_workspace_size",
-            "nf4_last_error", "nf4_status_string", "nf4_version"} <= set(names)
+            "nf4_last_error", "nf4_status_string", "nf4_version", "nf4_launch_count"} <= set(names)
     lib = ctypes.CDLL(nf4.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -52,6 +52,7 @@ def test_status_strings_and_version():
         assert nf4.nf4_status_string(code) == name
     assert nf4.nf4_status_string(99) == "NF4_ERR_UNKNOWN"
     assert nf4.nf4_version() >= 100
+    assert nf4.nf4_launch_count() >= 0
 
 
 FAKE = 1 << 20   # a 16-byte aligned non-null address; never dereferenced by these calls

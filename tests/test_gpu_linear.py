@@ -1,0 +1,207 @@
+"""GPU parity of nf4_linear against the CPU oracle.
+
+nf4_linear accumulates in fp32 in its own order, so it is compared within a
+tolerance: per output row m, max_n |Y - Yref| / ||Yref[m, :]||_2 <= 1e-2, with
+Yref the oracle's fp64 product of X and the dequantized weight.  A second,
+much tighter per-element bound is also checked -- bf16 output rounding plus
+fp32 summation error:
+
+    |Y - Yref| <= 2^-8 |Yref| + K * 2^-23 * sum_k |x_k| |w_k|   (+ tiny)
+
+which a dropped K-slice, a wrong scale or a transposed tile would break.
+W is always quantized by the oracle; the GPU only multiplies.  Large
+workloads are checked on seeded row samples (rows of Y are independent).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import nf4_weight_quantized_quantize_gb300 as nf4
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 1e-2
+
+
+def f32_of_bits(b):
+    return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
+
+
+def row_err(y, yref):
+    nrm = np.linalg.norm(yref, axis=1, keepdims=True)
+    return float(np.max(np.abs(y - yref) / np.maximum(nrm, 1e-300)))
+
+
+def check_bound(y, yref, x_bits, wdeq_f64):
+    K = x_bits.shape[1]
+    ax = np.abs(f32_of_bits(x_bits).astype(np.float64))
+    mag = ax @ np.abs(wdeq_f64).T
+    bound = 2.0 ** -8 * np.abs(yref) + K * 2.0 ** -23 * mag + 1e-30
+    viol = np.abs(y - yref) > bound
+    assert not viol.any(), f"{int(viol.sum())} elements exceed the rounding bound"
+
+
+class Quantized:
+    def __init__(self, w_bits_2d):
+        self.n, self.k = w_bits_2d.shape
+        self.p, self.a = oracle.quantize(w_bits_2d)
+        self.pd = torch.from_numpy(self.p).to(DEV)
+        self.ad = torch.from_numpy(self.a).to(DEV)
+        self._wdeq = None
+
+    def wdeq(self):
+        if self._wdeq is None:
+            d = oracle.dequantize(self.p, self.a, self.n * self.k)
+            self._wdeq = f32_of_bits(d).astype(np.float64).reshape(self.n, self.k)
+        return self._wdeq
+
+
+def run_linear(x_bits, q):
+    x = workloads.from_bits(x_bits, DEV)
+    y = nf4.linear(x, q.pd, q.ad, q.n)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def check(x_bits, q, rows=None, bound=True):
+    y = run_linear(x_bits, q)
+    xs = x_bits if rows is None else x_bits[rows]
+    ys = y if rows is None else y[rows]
+    yref = oracle.linear(xs, q.p, q.a, q.n)
+    err = row_err(ys, yref)
+    assert err <= TOL, f"row-normalised error {err}"
+    if bound:
+        check_bound(ys, yref, xs, q.wdeq())
+    return y, err
+
+
+def rand_bits(shape, std, seed):
+    rs = np.random.default_rng(seed)
+    t = torch.from_numpy((rs.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- the five workloads
+
+
+def test_tiny_full():
+    cfg = workloads.TINY
+    q = Quantized(workloads.bits(workloads.make_weight(cfg)))
+    check(workloads.bits(workloads.make_activation(cfg)), q)
+
+
+@pytest.mark.parametrize("cfg", [workloads.Q_PROJ, workloads.GATE_UP, workloads.DOWN], ids=lambda c: c.name)
+def test_projection_m2048_sampled_rows(cfg):
+    q = Quantized(workloads.bits(workloads.make_weight(cfg)))
+    x = workloads.bits(workloads.make_activation(cfg))
+    rs = np.random.default_rng(cfg.x_seed)
+    rows = np.sort(rs.choice(cfg.m, 48, replace=False))
+    rows[0] = 0
+    rows[-1] = cfg.m - 1
+    check(x, q, rows=rows, bound=(cfg.n * cfg.k <= 4096 * 3840 * 4))
+
+
+def test_down_proj_skinny_full():
+    cfg = workloads.DOWN_SKINNY
+    q = Quantized(workloads.bits(workloads.make_weight(cfg)))
+    x = workloads.bits(workloads.make_activation(cfg))
+    check(x, q)
+
+
+def test_skinny_rows_equal_rows_of_full_batch():
+    """Batched-vs-solo: the 16-row call (skinny kernel) matches the same 16 rows
+    of the 2048-row call (tile kernel) to within fp32 reordering + bf16 rounding."""
+    q = Quantized(workloads.bits(workloads.make_weight(workloads.DOWN)))
+    xf = workloads.bits(workloads.make_activation(workloads.DOWN))
+    xs = workloads.bits(workloads.make_activation(workloads.DOWN_SKINNY))
+    assert np.array_equal(xs, xf[:16])
+    yf = run_linear(xf, q)[:16]
+    ys = run_linear(xs, q)
+    scale = np.linalg.norm(yf, axis=1, keepdims=True)
+    assert np.max(np.abs(yf - ys) / scale) < 1e-3
+
+
+# ---------------------------------------------------------------- shapes and edges
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 256, 64), (256, 256, 128), (130, 256, 192), (255, 512, 256), (257, 300, 128),
+    (384, 264, 640), (512, 1000, 320), (129, 8, 64), (200, 200, 448), (1000, 768, 1024),
+])
+def test_tile_path_ragged_shapes(M, N, K):
+    q = Quantized(rand_bits((N, K), 0.02, M * 7 + N))
+    check(rand_bits((M, K), 1.0, M + K), q)
+
+
+@pytest.mark.parametrize("M", [1, 2, 7, 15, 16, 17, 31, 33, 48, 64, 65, 100, 112, 127])
+def test_skinny_path_all_widths(M):
+    N, K = 640, 1536
+    q = Quantized(rand_bits((N, K), 0.02, 1000 + M))
+    check(rand_bits((M, K), 1.0, 2000 + M), q)
+
+
+@pytest.mark.parametrize("N,K", [(64, 64), (72, 128), (1000, 64 * 50), (3840, 15360)])
+def test_skinny_path_shapes(N, K):
+    q = Quantized(rand_bits((N, K), 0.02, N + K))
+    check(rand_bits((16, K), 1.0, K), q, bound=(N * K <= 1 << 22))
+
+
+def test_outlier_weights_and_large_activations():
+    w = rand_bits((512, 1024), 0.02, 5).copy()
+    flat = w.reshape(-1)
+    idx = np.arange(0, flat.size, 997)
+    flat[idx] = rand_bits((idx.size,), 0.4, 6)
+    q = Quantized(w)
+    check(rand_bits((256, 1024), 30.0, 7), q)
+
+
+def test_zero_weight_blocks_give_zero_output():
+    w = np.zeros((256, 512), np.uint16)
+    q = Quantized(w)
+    y = run_linear(rand_bits((128, 512), 1.0, 8), q)
+    assert np.all(y == 0)
+
+
+def test_deterministic():
+    cfg = workloads.TINY
+    q = Quantized(workloads.bits(workloads.make_weight(cfg)))
+    for m in (16, 300):
+        x = rand_bits((m, cfg.k), 1.0, m)
+        assert np.array_equal(run_linear(x, q), run_linear(x, q))
+
+
+def test_matches_cublas_on_dequantized_weight():
+    """Against torch.matmul (cuBLAS) of the same dequantized bf16 weight: both
+    are fp32-accumulated, so they agree to about one bf16 rounding."""
+    cfg = workloads.Q_PROJ
+    q = Quantized(workloads.bits(workloads.make_weight(cfg)))
+    x = workloads.make_activation(cfg).to(DEV)
+    wd = workloads.from_bits(oracle.dequantize(q.p, q.a, q.n * q.k), DEV).view(q.n, q.k)
+    y = nf4.linear(x, q.pd, q.ad, q.n).float()
+    ref = torch.matmul(x, wd.t()).float()
+    diff = (y - ref).abs()
+    tol = 2.0 ** -7 * ref.abs() + 1e-3
+    frac_bad = (diff > tol).float().mean().item()
+    assert frac_bad < 1e-3, frac_bad
+
+
+def test_workspace_reuse_and_user_workspace():
+    N, K, M = 512, 2048, 16
+    q = Quantized(rand_bits((N, K), 0.02, 9))
+    x = workloads.from_bits(rand_bits((M, K), 1.0, 10), DEV)
+    st, need = nf4.nf4_linear_workspace_size(M, N, K)
+    assert st == nf4.NF4_OK and need > 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)   # garbage contents are fine
+    y1 = nf4.linear(x, q.pd, q.ad, N, workspace=ws)
+    y2 = nf4.linear(x, q.pd, q.ad, N, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(nf4.NF4Error):
+        nf4.linear(x, q.pd, q.ad, N, workspace=small)
+
+
+def test_no_error_recorded():
+    assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
