@@ -133,6 +133,33 @@ NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uin
  * call).  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad arguments. */
 NF4_API nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
+/*
+ * nf4_linear_noalloc -- nf4_linear for M < 128 that needs no caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory themselves (for example a plugin whose host
+ * application owns the whole device memory pool and forbids extensions from
+ * allocating, or a path where cudaMalloc's implicit device synchronization is
+ * not acceptable).  It computes what nf4_linear computes for the same
+ * arguments, with the split-K scratch in a fixed library-owned device array of
+ * NF4_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   x, M, K, packed, absmax, N, block, y, stream: as for nf4_linear, M < 128.
+ *
+ * Errors: M >= 128 -> NF4_ERR_SHAPE (nf4_linear needs no workspace there);
+ * a shape whose scratch (nf4_linear_workspace_size) exceeds
+ * NF4_NOALLOC_SCRATCH_BYTES -> NF4_ERR_WORKSPACE; otherwise as nf4_linear.
+ * The first call on a device resolves the array's device address (one
+ * cudaGetSymbolAddress with that device current): make it before any stream
+ * capture.  All calls on a device share the array: calls that overlap on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller.  Nothing in the array needs clearing between calls.
+ */
+#define NF4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+NF4_API nf4_status nf4_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                                      const float* absmax, int64_t N, int32_t block, uint16_t* y,
+                                      void* stream);
+
 /* Synchronize `stream`, then read and clear this device's error word.
  * Returns NF4_OK, NF4_ERR_TIMEOUT (a kernel gave up on a wait), or
  * NF4_ERR_CUDA if the synchronization itself failed. */

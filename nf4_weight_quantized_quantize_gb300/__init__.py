@@ -3,7 +3,7 @@
 Two layers, both argument marshalling only -- every step of the computation
 runs in the library's CUDA kernels:
 
-* ``nf4_quantize``, ``nf4_dequantize``, ``nf4_linear``,
+* ``nf4_quantize``, ``nf4_dequantize``, ``nf4_linear``, ``nf4_linear_noalloc``,
   ``nf4_linear_workspace_size``, ``nf4_last_error``, ``nf4_status_string``:
   the C entry points of ``include/nf4.h`` under the same names, taking plain
   integers (device addresses, sizes, a stream handle) and returning the
@@ -52,6 +52,7 @@ def _load():
         "nf4_status_string": [ctypes.c_int],
         "nf4_version": [],
         "nf4_launch_count": [],
+        "nf4_linear_noalloc": [P, I64, I64, P, P, I64, I32, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -93,6 +94,14 @@ def nf4_dequantize(packed: int, absmax: int, numel: int, block: int, out: int, s
 def nf4_linear(x: int, M: int, K: int, packed: int, absmax: int, N: int, block: int, y: int,
                workspace: int, workspace_bytes: int, stream: int = 0) -> int:
     return lib().nf4_linear(x, M, K, packed, absmax, N, block, y, workspace, workspace_bytes, stream)
+
+
+def nf4_linear_noalloc(x: int, M: int, K: int, packed: int, absmax: int, N: int, block: int, y: int,
+                       stream: int = 0) -> int:
+    return lib().nf4_linear_noalloc(x, M, K, packed, absmax, N, block, y, stream)
+
+
+NF4_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def nf4_linear_workspace_size(M: int, N: int, K: int) -> tuple[int, int]:

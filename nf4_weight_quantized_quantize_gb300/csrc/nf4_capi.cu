@@ -73,6 +73,8 @@ std::atomic<uint64_t> g_launches{0};
 
 void nf4::count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
+int nf4::current_device_info(const nf4::DeviceInfo** out) { return current_device(out); }
+
 extern "C" {
 
 nf4_status nf4_quantize(const uint16_t* w, int64_t numel, int32_t block, uint8_t* packed,

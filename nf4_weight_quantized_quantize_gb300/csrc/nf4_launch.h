@@ -21,6 +21,10 @@ struct DeviceInfo {
 // Add n to the process-wide count of enqueued kernels (nf4_launch_count).
 void count_launches(int n);
 
+// The current device's cached info (initialised on first use, see
+// nf4_capi.cu).  Returns 0 (NF4_OK) or an nf4_status code.
+int current_device_info(const DeviceInfo** out);
+
 cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t numel, uint8_t* packed,
                             float* absmax, cudaStream_t s);
 
