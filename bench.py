@@ -50,7 +50,7 @@ FLOPS_PER_STEP = 2 * CFG.m * CFG.n * CFG.k + 2 * SKINNY_M * CFG.n * CFG.k
 BYTES_PER_W_QUANT = 2.5625
 BYTES_PER_W_DEQUANT = 2.5625
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-CPU_SAMPLE_ROWS = 1024          # cpu_baseline: linear on this many of the 2048 rows
+CPU_SAMPLE_SECONDS = 10.0       # cpu_baseline: repeat the oracle step for at least this long
 REF_STEP_ROWS = 128             # reference arm: rows of X per step
 
 
@@ -208,15 +208,19 @@ def oracle_sample(rows: int, x_bits, w_bits):
     return 2 * (rows + SKINNY_M) * CFG.n * CFG.k, dt
 
 
-def cpu_baseline(rows: int = CPU_SAMPLE_ROWS):
+def cpu_baseline(min_seconds: float = CPU_SAMPLE_SECONDS):
+    """The oracle on the whole step (all rows), repeated until `min_seconds` of CPU work."""
     import oracle
     w = workloads.bits(workloads.make_weight(CFG))
     x = workloads.bits(workloads.make_activation(CFG))
-    flops, dt = oracle_sample(rows, x, w)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": (f"quantize + dequantize of the full W [{CFG.n}, {CFG.k}], linear on {rows} of the "
-                       f"{CFG.m} rows of X plus the {SKINNY_M}-row skinny batch; fp64 accumulation; "
-                       f"{dt:.2f} s")}
+    flops, secs, reps = 0, 0.0, 0
+    while secs < min_seconds:
+        f, dt = oracle_sample(CFG.m, x, w)
+        flops, secs, reps = flops + f, secs + dt, reps + 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"{reps} x the whole step (quantize + dequantize of W [{CFG.n}, {CFG.k}], linear on all "
+                       f"{CFG.m} rows of X and on the {SKINNY_M}-row batch), fp64 accumulation, "
+                       f"{secs:.1f} s")}
 
 
 def run_reference(args):
