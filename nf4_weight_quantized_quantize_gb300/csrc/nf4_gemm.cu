@@ -37,36 +37,76 @@ namespace nf4 {
 
 constexpr int kBK = 64;                    // K per pipeline stage = one NF4 block = one 128-byte row
 constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per stage
+constexpr int kLutCopies = 32;             // one copy of the byte LUT per lane
+constexpr int kLutBytes = 256 * kLutCopies * 4;   // 32 KB
 
+// Barriers of both kernels, in shared memory:
+//   full[s1]  TMA landed (activations + packed weights of a K-slice)
+//   empty[s1] the MMA of that K-slice completed: its ring slot may be refilled
+//   conv[s2]  converter warps finished a converted-weight buffer
+//   cfree[s2] the MMA reading that converted buffer completed
+//   accum     the accumulator is final; drain: used only on the error path
 struct Barriers {
-    // layout in shared memory: full[S], conv[S], empty[S], accum, drain
     uint32_t base;
-    int stages;
+    int s1, s2;
     __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t conv(int s) const { return base + 8u * (stages + s); }
-    __device__ uint32_t empty(int s) const { return base + 8u * (2 * stages + s); }
-    __device__ uint32_t accum() const { return base + 8u * (3 * stages); }
-    __device__ uint32_t drain() const { return base + 8u * (3 * stages + 1); }
+    __device__ uint32_t empty(int s) const { return base + 8u * (s1 + s); }
+    __device__ uint32_t conv(int b) const { return base + 8u * (2 * s1 + b); }
+    __device__ uint32_t cfree(int b) const { return base + 8u * (2 * s1 + s2 + b); }
+    __device__ uint32_t accum() const { return base + 8u * (2 * s1 + 2 * s2); }
+    __device__ uint32_t drain() const { return base + 8u * (2 * s1 + 2 * s2 + 1); }
+    __host__ __device__ static constexpr int count(int a, int b) { return 2 * a + 2 * b + 2; }
 };
 
-// Convert one weight row of one stage: 32 packed bytes (64 elements) at
-// `prow` to 64 bf16 at `brow` in the 128-byte swizzle (16-byte chunk c of row
-// r stored at chunk position c ^ (r & 7)).  Chunk c holds packed word c.
-__device__ __forceinline__ void convert_row(const uint8_t* prow, uint8_t* brow, int r,
-                                            const uint32_t* lut, float am) {
-    const uint4 q0 = *reinterpret_cast<const uint4*>(prow);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(prow + 16);
-    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint32_t p = words[c];
-        uint4 o;
-        o.x = scale_entry(lut[p & 0xffu], am);
-        o.y = scale_entry(lut[(p >> 8) & 0xffu], am);
-        o.z = scale_entry(lut[(p >> 16) & 0xffu], am);
-        o.w = scale_entry(lut[p >> 24], am);
-        *reinterpret_cast<uint4*>(brow + ((c ^ (r & 7)) << 4)) = o;
+// full[s] completes on the TMA bytes plus kFullArrivals arrivals: the
+// producer lane's expect-tx arrive and one cp.async arrive per producer lane.
+constexpr int kFullArrivals = 1 + 32;
+
+__device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arrivals) {
+    for (int s = 0; s < bar.s1; ++s) {
+        mbar_init(bar.full(s), kFullArrivals);
+        mbar_init(bar.empty(s), 1);
     }
+    for (int b = 0; b < bar.s2; ++b) {
+        mbar_init(bar.conv(b), conv_arrivals);
+        mbar_init(bar.cfree(b), 1);
+    }
+    mbar_init(bar.accum(), 1);
+    mbar_init(bar.drain(), 1);
+}
+
+// The byte LUT replicated once per lane: word (b * 32 + lane) holds the
+// bf16x2 codebook pair of byte b.  Lane l only reads copy l, which lives in
+// bank l, so the 32 random lookups of a warp never conflict.
+__device__ __forceinline__ void build_lut(uint32_t* lut, int tid, int nthreads) {
+    for (int i = tid; i < 256 * kLutCopies; i += nthreads) lut[i] = lut_entry(static_cast<uint32_t>(i) >> 5);
+}
+
+// bf16x2 multiply with one round-to-nearest-even per half.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Eight weights (one packed 32-bit word, bytes in address order) to four
+// bf16x2 words.  The scale enters as bf16x2 `am2`; a bf16 x bf16 product is
+// exact in fp32, so each half equals bf16_rne(float(bf16(C)) * absmax) -- the
+// dequantizer's value -- whenever absmax is a bf16 value, which every absmax
+// nf4_quantize writes is (the max of bf16 magnitudes).
+__device__ __forceinline__ uint4 expand8(uint32_t p, const uint32_t* lut_lane, uint32_t am2) {
+    uint4 o;
+    o.x = bf16x2_mul(lut_lane[(p & 0xffu) * kLutCopies], am2);
+    o.y = bf16x2_mul(lut_lane[((p >> 8) & 0xffu) * kLutCopies], am2);
+    o.z = bf16x2_mul(lut_lane[((p >> 16) & 0xffu) * kLutCopies], am2);
+    o.w = bf16x2_mul(lut_lane[(p >> 24) * kLutCopies], am2);
+    return o;
+}
+
+// Store one 16-byte chunk c of row r of a 128-byte-swizzled K-major tile
+// (the layout TMA's 128-byte swizzle produces and the MMA descriptor reads).
+__device__ __forceinline__ void st_sw128(uint8_t* tile, int r, int c, uint4 v) {
+    *reinterpret_cast<uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4)) = v;
 }
 
 // Whether a converter warp reports K-slice kb as converted.  Always true in
@@ -83,35 +123,84 @@ __device__ __forceinline__ bool report_converted(int kb) {
 #endif
 }
 
-// Wait (bounded) for the copies a producer issued into the last `stages`
+// Wait (bounded) for the copies a producer issued into the last `s1`
 // K-slices to land, so no TMA write targets shared memory after exit.
-__device__ __forceinline__ void drain_tma(const Barriers& bar, int issued, int stages,
-                                          uint32_t* err, volatile int* abort_flag) {
+__device__ __forceinline__ void drain_tma(const Barriers& bar, int issued, uint32_t* err) {
+    int dummy = 0;   // a fresh flag: the CTA-wide abort is already raised here
+    for (int kb = max(0, issued - bar.s1); kb < issued; ++kb)
+        if (!mbar_wait(bar.full(kb % bar.s1), (kb / bar.s1) & 1, err, &dummy, kErrTimeoutDrain)) break;
+}
+
+// Error-path exit of the MMA issuer: wait (bounded) until every MMA it issued
+// has completed, so TMEM can be released.
+__device__ __forceinline__ void drain_mma(const Barriers& bar, uint32_t* err) {
     int dummy = 0;
-    for (int kb = max(0, issued - stages); kb < issued; ++kb) {
-        const int s = kb % stages;
-        // a fresh local flag: the CTA-wide abort is already raised here
-        if (!mbar_wait(bar.full(s), (kb / stages) & 1, err, &dummy, kErrTimeoutDrain)) break;
+    mma_commit(bar.drain());
+    mbar_wait(bar.drain(), 0, err, &dummy, kErrTimeoutDrain);
+}
+
+// Producer warp, one K-slice: lane 0 arms full[s] with the TMA byte count and
+// issues the two tile loads; every lane copies the scales of rows
+// lane, lane + 32, ... of the slice into `am_dst` with 4-byte cp.async and
+// arrives on full[s] when its copies land.  Rows past N copy a harmless
+// in-range scale (their outputs are never stored).
+template <int ROWS>
+__device__ __forceinline__ void produce_slice(const Barriers& bar, int s, int lane, uint32_t tx_bytes,
+                                              const CUtensorMap* tm_x, uint32_t x_dst, int x_col, int x_row,
+                                              const CUtensorMap* tm_w, uint32_t p_dst, int p_col, int n0,
+                                              uint32_t am_dst, const float* absmax, int N, int64_t am_pitch,
+                                              int kb_abs) {
+    if (lane == 0) {
+        mbar_arrive_expect_tx(bar.full(s), tx_bytes);
+        tma_load_2d(x_dst, tm_x, bar.full(s), x_col, x_row);
+        tma_load_2d(p_dst, tm_w, bar.full(s), p_col, n0);
     }
-    (void)abort_flag;
+#pragma unroll
+    for (int i = lane; i < ROWS; i += 32) {
+        const int n = n0 + i;
+        const float* src = absmax + (n < N ? static_cast<int64_t>(n) * am_pitch + kb_abs : 0);
+        cp_async_4(am_dst + 4u * i, src);
+    }
+    cp_async_arrive_noinc(bar.full(s));
 }
 
 // ============================================================ large-M kernel
 
+#ifndef NF4_BIG_S1
+#define NF4_BIG_S1 3
+#endif
+#ifndef NF4_BIG_S2
+#define NF4_BIG_S2 2
+#endif
+#ifndef NF4_BIG_CONV_WARPS
+#define NF4_BIG_CONV_WARPS 16
+#endif
+
 namespace big {
 constexpr int BM = 256;
 constexpr int BN = 256;
-constexpr int STAGES = 3;
-constexpr int A_BYTES = BM * kBK * 2;        // 32 KB
+constexpr int S1 = NF4_BIG_S1;               // activation + packed-weight + scale ring
+constexpr int S2 = NF4_BIG_S2;               // converted-weight buffers
+constexpr int X_BYTES = BM * kBK * 2;        // 32 KB
 constexpr int B_BYTES = BN * kBK * 2;        // 32 KB
 constexpr int P_BYTES = BN * kPackedRow;     // 8 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + P_BYTES;
-constexpr int CONV_WARPS = BN / 32;          // one converter thread per weight row
+constexpr int AM_BYTES = BN * 4;             // 1 KB of fp32 scales
+constexpr int CONV_WARPS = NF4_BIG_CONV_WARPS;   // 8: one converter thread per weight row, 16: two
+constexpr int ROW_SPLIT = CONV_WARPS / 8;    // converter threads per weight row
+constexpr int COL_SPLIT = CONV_WARPS / 8;    // epilogue warps per (accumulator, lane quarter)
 constexpr int THREADS = 64 + CONV_WARPS * 32;
 constexpr int TMEM_COLS = 512;               // two 128 x 256 fp32 accumulators
-constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 1024 + 256;
+constexpr int OFF_X = 0;
+constexpr int OFF_B = OFF_X + S1 * X_BYTES;
+constexpr int OFF_P = OFF_B + S2 * B_BYTES;
+constexpr int OFF_LUT = OFF_P + S1 * P_BYTES;
+constexpr int OFF_AM = OFF_LUT + kLutBytes;
+constexpr int OFF_BAR = OFF_AM + S1 * AM_BYTES;
+constexpr int NUM_BARS = Barriers::count(S1, S2);
+constexpr size_t SMEM = 1024 + OFF_BAR + NUM_BARS * 8 + 16;
 static_assert(SMEM <= 232448, "shared memory budget");
-static_assert(CONV_WARPS == 8, "epilogue maps 8 warps onto 2 accumulators x 4 lane quarters");
+static_assert(OFF_B % 1024 == 0 && X_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
+static_assert(CONV_WARPS == 8 || CONV_WARPS == 16, "converter warps: 8 or 16");
 }  // namespace big
 
 struct GemmArgs {
@@ -127,15 +216,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     using namespace big;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(lut + 256);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + 3 * STAGES + 2);
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + OFF_LUT);
+    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const Barriers bar{smem_u32(bar_mem), STAGES};
+    const Barriers bar{smem_u32(bar_mem), S1, S2};
 
-    auto a_tile = [&](int s) { return smem + s * STAGE_BYTES; };
-    auto b_tile = [&](int s) { return smem + s * STAGE_BYTES + A_BYTES; };
-    auto p_tile = [&](int s) { return smem + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+    auto x_tile = [&](int s) { return smem + OFF_X + s * X_BYTES; };
+    auto b_tile = [&](int b) { return smem + OFF_B + b * B_BYTES; };
+    auto p_tile = [&](int s) { return smem + OFF_P + s * P_BYTES; };
+    auto am_tile = [&](int s) { return reinterpret_cast<const float*>(smem + OFF_AM + s * AM_BYTES); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -146,13 +236,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int nk = args.K / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar.full(s), 1);
-            mbar_init(bar.conv(s), CONV_WARPS);
-            mbar_init(bar.empty(s), 1);
-        }
-        mbar_init(bar.accum(), 1);
-        mbar_init(bar.drain(), 1);
+        init_barriers(bar, CONV_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -164,45 +248,41 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp >= 2) {
-        for (int e = threadIdx.x - 64; e < 256; e += CONV_WARPS * 32) lut[e] = lut_entry(e);
-    }
+    if (warp >= 2) build_lut(lut, threadIdx.x - 64, CONV_WARPS * 32);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait(bar.empty(s), ((kb / STAGES) - 1) & 1, args.err, abort_flag,
-                                               kErrTimeoutEmpty))
-                    break;
-                if (*abort_flag) break;
-                mbar_arrive_expect_tx(bar.full(s), A_BYTES + P_BYTES);
-                tma_load_2d(smem_u32(a_tile(s)), &tm_x, bar.full(s), kb * kBK, m0);
-                tma_load_2d(smem_u32(p_tile(s)), &tm_w, bar.full(s), kb * kPackedRow, n0);
-                ++issued;
-            }
-            if (*abort_flag) drain_tma(bar, issued, STAGES, args.err, abort_flag);
+        // ---------------- producer warp
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S1;
+            bool ok = true;
+            if (kb >= S1)
+                ok = mbar_wait(bar.empty(s), ((kb / S1) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
+            produce_slice<BN>(bar, s, lane, X_BYTES + P_BYTES, &tm_x, smem_u32(x_tile(s)), kb * kBK, m0, &tm_w,
+                              smem_u32(p_tile(s)), kb * kPackedRow, n0, smem_u32(am_tile(s)), args.absmax, args.N,
+                              nk, kb);
+            ++issued;
         }
+        if (*abort_flag && lane == 0) drain_tma(bar, issued, args.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
             bool ok = true;
             for (int kb = 0; kb < nk && ok; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t par = (kb / STAGES) & 1;
-                ok = mbar_wait(bar.full(s), par, args.err, abort_flag, kErrTimeoutFull) &&
-                     mbar_wait(bar.conv(s), par, args.err, abort_flag, kErrTimeoutConverted);
+                const int s = kb % S1;
+                const int b = kb % S2;
+                ok = mbar_wait(bar.full(s), (kb / S1) & 1, args.err, abort_flag, kErrTimeoutFull) &&
+                     mbar_wait(bar.conv(b), (kb / S2) & 1, args.err, abort_flag, kErrTimeoutConverted);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(a_tile(s));
-                const uint32_t b0 = smem_u32(b_tile(s));
+                const uint32_t a0 = smem_u32(x_tile(s));
+                const uint32_t b0 = smem_u32(b_tile(b));
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j) {
                     const uint64_t bd = smem_desc_sw128(b0 + 32 * j);
@@ -211,68 +291,78 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     mma_bf16(tmem + BN, smem_desc_sw128(a0 + 128 * 128 + 32 * j), bd, idesc, acc);
                 }
                 mma_commit(bar.empty(s));
+                mma_commit(bar.cfree(b));
             }
-            if (ok) {
+            if (ok)
                 mma_commit(bar.accum());
-            } else {
-                int dummy = 0;
-                mma_commit(bar.drain());
-                mbar_wait(bar.drain(), 0, args.err, &dummy, kErrTimeoutDrain);
-            }
+            else
+                drain_mma(bar, args.err);
         }
     } else {
-        // ---------------- converters, then epilogue
-        const int r = threadIdx.x - 64;          // weight row within the tile
-        const int n = n0 + r;
-        const bool valid = n < args.N;
-        const float* am_row = args.absmax + static_cast<int64_t>(valid ? n : 0) * nk;
-        float am0 = valid ? ldg_nc_f32(am_row) : 0.0f;
-        float am1 = (valid && nk > 1) ? ldg_nc_f32(am_row + 1) : 0.0f;
+        // ---------------- converters (ROW_SPLIT per weight row), then epilogue
+        const int t = threadIdx.x - 64;
+        const int r = t & (BN - 1);              // weight row within the tile
+        const int h = t >> 8;                    // part of the slice: 32 / ROW_SPLIT packed bytes
+        const uint32_t* lut_lane = lut + lane;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % STAGES;
-            const float am = am0;
-            am0 = am1;
-            am1 = (valid && kb + 2 < nk) ? ldg_nc_f32(am_row + kb + 2) : 0.0f;
+            const int s = kb % S1;
+            const int b = kb % S2;
             // every lane polls; the outcome is made warp-uniform before anyone branches
-            const bool got = mbar_wait(bar.full(s), (kb / STAGES) & 1, args.err, abort_flag, kErrTimeoutFull);
+            bool got = mbar_wait(bar.full(s), (kb / S1) & 1, args.err, abort_flag, kErrTimeoutFull);
+            if (got && kb >= S2)
+                got = mbar_wait(bar.cfree(b), ((kb / S2) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
-            convert_row(p_tile(s) + r * kPackedRow, b_tile(s) + r * 128, r, lut, am);
+            const float am = am_tile(s)[r];
+            const uint32_t am2 = pack_bf16x2(am, am);
+            uint8_t* bt = b_tile(b);
+#pragma unroll
+            for (int part = 0; part < 2 / ROW_SPLIT; ++part) {
+                const int w16 = 2 / ROW_SPLIT * h + part;    // 16-byte packed word of the row
+                const uint4 q = *reinterpret_cast<const uint4*>(p_tile(s) + r * kPackedRow + 16 * w16);
+                st_sw128(bt, r, 4 * w16 + 0, expand8(q.x, lut_lane, am2));
+                st_sw128(bt, r, 4 * w16 + 1, expand8(q.y, lut_lane, am2));
+                st_sw128(bt, r, 4 * w16 + 2, expand8(q.z, lut_lane, am2));
+                st_sw128(bt, r, 4 * w16 + 3, expand8(q.w, lut_lane, am2));
+            }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(s));
+            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(b));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
+            const int cw = warp - 2;
             const int q = warp & 3;              // TMEM lane quarter this warp may access
-            const int acc = (warp - 2) >> 2;     // accumulator (M half)
+            const int acc = (cw >> 2) & 1;       // accumulator (M half)
+            const int ch = cw >> 3;              // column part of the tile (0 with 8 warps)
+            constexpr int COLS = BN / COL_SPLIT;
             const int row = m0 + acc * 128 + q * 32 + lane;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + ch * COLS;
             const bool vec = (args.N % 8) == 0;
             uint16_t* yrow = args.y + static_cast<int64_t>(row) * args.N;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 16) {
+            for (int c0 = 0; c0 < COLS; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();
-                uint32_t h[8];
+                uint32_t hv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) h[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                const int nc = n0 + c0;
+                for (int i = 0; i < 8; ++i) hv[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                const int nc = n0 + ch * COLS + c0;
                 if (row < args.M && nc < args.N) {
                     if (vec && nc + 16 <= args.N) {
-                        stg_v4(yrow + nc, make_uint4(h[0], h[1], h[2], h[3]));
-                        stg_v4(yrow + nc + 8, make_uint4(h[4], h[5], h[6], h[7]));
+                        stg_v4(yrow + nc, make_uint4(hv[0], hv[1], hv[2], hv[3]));
+                        stg_v4(yrow + nc + 8, make_uint4(hv[4], hv[5], hv[6], hv[7]));
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             if (nc + i < args.N)
-                                yrow[nc + i] = static_cast<uint16_t>(i & 1 ? h[i >> 1] >> 16 : h[i >> 1] & 0xffffu);
+                                yrow[nc + i] = static_cast<uint16_t>(i & 1 ? hv[i >> 1] >> 16 : hv[i >> 1] & 0xffffu);
                     }
                 }
             }
@@ -289,18 +379,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ============================================================ skinny kernel
 
+#ifndef NF4_SKINNY_SA
+#define NF4_SKINNY_SA 3
+#endif
+
 namespace skinny {
 constexpr int BN = 128;                      // weight rows per CTA (MMA M)
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BN * kBK * 2;        // converted weight, 16 KB
+constexpr int SA = NF4_SKINNY_SA;            // converted-weight buffers
+constexpr int A_BYTES = BN * kBK * 2;        // 16 KB
 constexpr int P_BYTES = BN * kPackedRow;     // 4 KB
-constexpr int CONV_WARPS = BN / 32;          // 4
+constexpr int AM_BYTES = BN * 4;             // 512 B of fp32 scales
+constexpr int CONV_WARPS = 8;                // two threads per weight row
 constexpr int THREADS = 64 + CONV_WARPS * 32;
 constexpr int TARGET_CTAS = 152;             // one wave on a GB300 (152 SMs)
+// shared memory left for the activation + packed + scale ring
+constexpr int RING_BUDGET = 232448 - 1024 - SA * A_BYTES - kLutBytes - 2048;
 __host__ __device__ constexpr int x_bytes(int mpad) { return mpad * kBK * 2; }
-__host__ __device__ constexpr int stage_bytes(int mpad) { return A_BYTES + P_BYTES + x_bytes(mpad); }
+__host__ __device__ constexpr int slot_bytes(int mpad) { return P_BYTES + x_bytes(mpad) + AM_BYTES; }
+__host__ __device__ constexpr int stages(int mpad) {
+    return RING_BUDGET / slot_bytes(mpad) > 16 ? 16 : RING_BUDGET / slot_bytes(mpad);
+}
 __host__ __device__ constexpr int tmem_cols(int mpad) { return mpad <= 32 ? 32 : mpad <= 64 ? 64 : 128; }
-inline size_t smem_bytes(int mpad) { return 1024 + size_t(STAGES) * stage_bytes(mpad) + 1024 + 256; }
+__host__ __device__ constexpr int off_x() { return SA * A_BYTES; }
+__host__ __device__ constexpr int off_p(int mpad) { return off_x() + stages(mpad) * x_bytes(mpad); }
+__host__ __device__ constexpr int off_am(int mpad) { return off_p(mpad) + stages(mpad) * P_BYTES; }
+__host__ __device__ constexpr int off_lut(int mpad) { return off_am(mpad) + stages(mpad) * AM_BYTES; }
+__host__ __device__ constexpr int off_bar(int mpad) { return off_lut(mpad) + kLutBytes; }
+__host__ __device__ constexpr size_t smem_bytes(int mpad) {
+    return 1024 + off_bar(mpad) + Barriers::count(stages(mpad), SA) * 8 + 16;
+}
+static_assert(smem_bytes(16) <= 232448 && smem_bytes(128) <= 232448, "shared memory budget");
 }  // namespace skinny
 
 // Split-K plan of the skinny path: a pure function of the shape, so the
@@ -333,21 +441,23 @@ __global__ void __launch_bounds__(skinny::THREADS, 1)
 skinny_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
               const SkinnyArgs args) {
     using namespace skinny;
+    constexpr int S1 = stages(MPAD);
     constexpr int XB = x_bytes(MPAD);
-    constexpr int SB = stage_bytes(MPAD);
     constexpr int TCOLS = tmem_cols(MPAD);
+    constexpr int NUM_BARS = Barriers::count(S1, SA);
+    static_assert(off_x() % 1024 == 0 && XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + STAGES * SB);
-    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(lut + 256);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + 3 * STAGES + 2);
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + off_lut(MPAD));
+    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + off_bar(MPAD));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const Barriers bar{smem_u32(bar_mem), STAGES};
+    const Barriers bar{smem_u32(bar_mem), S1, SA};
 
-    // stage layout: converted weight (1024-aligned), activations (1024-aligned), packed
-    auto a_tile = [&](int s) { return smem + s * SB; };
-    auto x_tile = [&](int s) { return smem + s * SB + A_BYTES; };
-    auto p_tile = [&](int s) { return smem + s * SB + A_BYTES + XB; };
+    auto a_tile = [&](int b) { return smem + b * A_BYTES; };
+    auto x_tile = [&](int s) { return smem + off_x() + s * XB; };
+    auto p_tile = [&](int s) { return smem + off_p(MPAD) + s * P_BYTES; };
+    auto am_tile = [&](int s) { return reinterpret_cast<const float*>(smem + off_am(MPAD) + s * AM_BYTES); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -358,13 +468,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     const int nk = min(args.kb_per_split, nk_total - kb0);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar.full(s), 1);
-            mbar_init(bar.conv(s), CONV_WARPS);
-            mbar_init(bar.empty(s), 1);
-        }
-        mbar_init(bar.accum(), 1);
-        mbar_init(bar.drain(), 1);
+        init_barriers(bar, CONV_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -376,84 +480,81 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         tmem_alloc(smem_u32(tmem_slot), TCOLS);
         tmem_relinquish();
     }
-    if (warp >= 2) {
-        for (int e = threadIdx.x - 64; e < 256; e += CONV_WARPS * 32) lut[e] = lut_entry(e);
-    }
+    if (warp >= 2) build_lut(lut, threadIdx.x - 64, CONV_WARPS * 32);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait(bar.empty(s), ((kb / STAGES) - 1) & 1, args.err, abort_flag,
-                                               kErrTimeoutEmpty))
-                    break;
-                if (*abort_flag) break;
-                mbar_arrive_expect_tx(bar.full(s), XB + P_BYTES);
-                tma_load_2d(smem_u32(x_tile(s)), &tm_x, bar.full(s), (kb0 + kb) * kBK, 0);
-                tma_load_2d(smem_u32(p_tile(s)), &tm_w, bar.full(s), (kb0 + kb) * kPackedRow, n0);
-                ++issued;
-            }
-            if (*abort_flag) drain_tma(bar, issued, STAGES, args.err, abort_flag);
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S1;
+            bool ok = true;
+            if (kb >= S1)
+                ok = mbar_wait(bar.empty(s), ((kb / S1) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
+            produce_slice<BN>(bar, s, lane, XB + P_BYTES, &tm_x, smem_u32(x_tile(s)), (kb0 + kb) * kBK, 0, &tm_w,
+                              smem_u32(p_tile(s)), (kb0 + kb) * kPackedRow, n0, smem_u32(am_tile(s)), args.absmax,
+                              args.N, nk_total, kb0 + kb);
+            ++issued;
         }
+        if (*abort_flag && lane == 0) drain_tma(bar, issued, args.err);
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, MPAD);
             bool ok = true;
             for (int kb = 0; kb < nk && ok; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t par = (kb / STAGES) & 1;
-                ok = mbar_wait(bar.full(s), par, args.err, abort_flag, kErrTimeoutFull) &&
-                     mbar_wait(bar.conv(s), par, args.err, abort_flag, kErrTimeoutConverted);
+                const int s = kb % S1;
+                const int b = kb % SA;
+                ok = mbar_wait(bar.full(s), (kb / S1) & 1, args.err, abort_flag, kErrTimeoutFull) &&
+                     mbar_wait(bar.conv(b), (kb / SA) & 1, args.err, abort_flag, kErrTimeoutConverted);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(a_tile(s));
+                const uint32_t a0 = smem_u32(a_tile(b));
                 const uint32_t x0 = smem_u32(x_tile(s));
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j)
                     mma_bf16(tmem, smem_desc_sw128(a0 + 32 * j), smem_desc_sw128(x0 + 32 * j), idesc,
                              (kb > 0 || j > 0) ? 1u : 0u);
                 mma_commit(bar.empty(s));
+                mma_commit(bar.cfree(b));
             }
-            if (ok) {
+            if (ok)
                 mma_commit(bar.accum());
-            } else {
-                int dummy = 0;
-                mma_commit(bar.drain());
-                mbar_wait(bar.drain(), 0, args.err, &dummy, kErrTimeoutDrain);
-            }
+            else
+                drain_mma(bar, args.err);
         }
     } else {
-        const int r = threadIdx.x - 64;
-        const int n = n0 + r;
-        const bool valid = n < args.N;
-        const float* am_row = args.absmax + static_cast<int64_t>(valid ? n : 0) * nk_total + kb0;
-        float am0 = valid ? ldg_nc_f32(am_row) : 0.0f;
-        float am1 = (valid && nk > 1) ? ldg_nc_f32(am_row + 1) : 0.0f;
+        // two converter threads per weight row: half h holds K elements [32h, 32h + 32)
+        const int r = (warp & 3) * 32 + lane;
+        const int h = (warp - 2) >> 2;
+        const uint32_t* lut_lane = lut + lane;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % STAGES;
-            const float am = am0;
-            am0 = am1;
-            am1 = (valid && kb + 2 < nk) ? ldg_nc_f32(am_row + kb + 2) : 0.0f;
-            // every lane polls; the outcome is made warp-uniform before anyone branches
-            const bool got = mbar_wait(bar.full(s), (kb / STAGES) & 1, args.err, abort_flag, kErrTimeoutFull);
+            const int s = kb % S1;
+            const int b = kb % SA;
+            bool got = mbar_wait(bar.full(s), (kb / S1) & 1, args.err, abort_flag, kErrTimeoutFull);
+            if (got && kb >= SA)
+                got = mbar_wait(bar.cfree(b), ((kb / SA) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
-            convert_row(p_tile(s) + r * kPackedRow, a_tile(s) + r * 128, r, lut, am);
+            const float am = am_tile(s)[r];
+            const uint32_t am2 = pack_bf16x2(am, am);
+            const uint4 q = *reinterpret_cast<const uint4*>(p_tile(s) + r * kPackedRow + 16 * h);
+            uint8_t* at = a_tile(b);
+            st_sw128(at, r, 4 * h + 0, expand8(q.x, lut_lane, am2));
+            st_sw128(at, r, 4 * h + 1, expand8(q.y, lut_lane, am2));
+            st_sw128(at, r, 4 * h + 2, expand8(q.z, lut_lane, am2));
+            st_sw128(at, r, 4 * h + 3, expand8(q.w, lut_lane, am2));
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(s));
+            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(b));
         }
-        // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
-        if (__all_sync(0xffffffffu, ok)) {
+        if (warp < 6 && __all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             // TMEM lane = weight row (n), column = activation row (m)
             const int q = warp & 3;

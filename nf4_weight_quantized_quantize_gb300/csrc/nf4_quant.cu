@@ -44,6 +44,80 @@ __device__ __forceinline__ uint32_t quantize8(uint4 v, uint32_t am_bits, const f
     return out;
 }
 
+// Fast code selection.  n = w / absmax is approximated by q = w * rcp(absmax)
+// with a correctly rounded reciprocal: |q - n| <= 3 * 2^-24 * |n|.  A uniform
+// grid of 65 cells of width 1/32 over [-1, 1] holds at most one threshold per
+// cell, and every threshold sits at least 1e-3 from a cell edge (checked at
+// compile time below), so the cell of q and the count of thresholds below it
+// are those of n.  Only the cell's own threshold can separate q from n, and
+// only when |q - t| <= 2^-20 |t|; such elements (a handful per billion) take
+// the exact path: IEEE division and the threshold search.
+constexpr int kCells = 65;
+constexpr double kCellWidth = 1.0 / 32.0;
+
+constexpr bool grid_is_safe() {
+    int prev_cell = -1;
+    for (int j = 0; j < 15; ++j) {
+        double t = static_cast<double>(threshold(j));
+        double x = (t + 1.0) / kCellWidth;
+        int cell = static_cast<int>(x);
+        double frac = x - cell;
+        if (cell <= prev_cell) return false;                      // one threshold per cell
+        if (frac * kCellWidth < 1e-3 || (1.0 - frac) * kCellWidth < 1e-3) return false;
+        prev_cell = cell;
+    }
+    return true;
+}
+static_assert(grid_is_safe(), "quantizer grid: thresholds must be one per cell and away from cell edges");
+
+struct QuantCell {
+    float t;          // the threshold inside the cell, or +inf
+    float guard;      // |t| * 2^-20: closer than this, decide exactly
+    uint32_t base;    // number of thresholds below the cell
+    uint32_t pad;
+};
+
+__device__ __forceinline__ void build_cells(QuantCell* cells, int tid, int nthreads) {
+    for (int i = tid; i < kCells; i += nthreads) {
+        const float lo = static_cast<float>(i) * 0.03125f - 1.0f;     // exact
+        const float hi = lo + 0.03125f;
+        QuantCell c{__int_as_float(0x7f800000), 0.0f, 0u, 0u};
+        for (int j = 0; j < 15; ++j) {
+            const float t = c_thr[j];
+            if (t < lo) ++c.base;
+            else if (t < hi) c.t = t, c.guard = fabsf(t) * 0x1p-20f;
+        }
+        cells[i] = c;
+    }
+}
+
+__device__ __forceinline__ uint32_t fast_code(float q, const QuantCell* cells, bool& exact_needed) {
+    int idx = __float2int_rz(fmaf(q, 32.0f, 32.0f));
+    idx = min(max(idx, 0), kCells - 1);
+    const QuantCell c = cells[idx];
+    exact_needed |= !(fabsf(q - c.t) > c.guard);
+    return c.base + (q > c.t ? 1u : 0u);
+}
+
+// quantize8 with the fast path: one reciprocal per block, the exact path only
+// for elements the grid cannot decide.
+__device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, const QuantCell* cells,
+                                                   const float* s_thr) {
+    if (am_bits == 0u) return 0x77777777u;
+    const float am = __uint_as_float(am_bits << 16);
+    const float rcp = __frcp_rn(am);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0;
+    bool exact_needed = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c0 = fast_code(__uint_as_float(wd[i] << 16) * rcp, cells, exact_needed);
+        const uint32_t c1 = fast_code(__uint_as_float(wd[i] & 0xffff0000u) * rcp, cells, exact_needed);
+        out |= ((c0 << 4) | c1) << (8 * i);
+    }
+    return exact_needed ? quantize8(v, am_bits, s_thr) : out;
+}
+
 __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
     uint32_t m = max(max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu), max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu));
     m = max(m, max(max(v.z & 0x7fffu, (v.z >> 16) & 0x7fffu), max(v.w & 0x7fffu, (v.w >> 16) & 0x7fffu)));
@@ -61,7 +135,9 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __restrict__ packed,
                     float* __restrict__ absmax) {
     __shared__ float s_thr[16];
+    __shared__ QuantCell s_cells[kCells];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
+    build_cells(s_cells, threadIdx.x, kQuantThreads);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
@@ -82,7 +158,7 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
             if (t0 + u * nwarps < ntiles && word < nwords) {
-                packed[word] = quantize8(v[u], m, s_thr);
+                packed[word] = quantize8_fast(v[u], m, s_cells, s_thr);
                 if ((lane & 7) == 0) absmax[word >> 3] = __uint_as_float(m << 16);
             }
         }

@@ -165,3 +165,45 @@ def test_stack_all_weights_sampled_rows():
             assert np.array_equal(ag.view(np.uint32), a_ref.view(np.uint32)), (layer, pi)
             assert np.array_equal(workloads.bits(y[ri]).ravel(), oracle.dequantize(p_ref, a_ref, wr.size))
     assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
+
+
+def _near_threshold_pairs(rel):
+    """bf16 (absmax, w) pairs whose fp32 quotient w / absmax lies within `rel`
+    (relative) of a decision midpoint between neighbouring codebook values."""
+    import numpy as np
+    cb = np.array(oracle.codebook(), dtype=np.float64)
+    mids = (cb[:-1] + cb[1:]) / 2
+    pairs = []
+    for am in (1 + np.arange(128) / 128).astype(np.float32):
+        for t in mids:
+            u = int(np.array([np.float32(t * am)]).view(np.uint32)[0])
+            for d in (-1, 0, 1):
+                w = np.array([(((u >> 16) + d) & 0xffff) << 16], dtype=np.uint32).view(np.float32)[0]
+                n = np.float32(w) / np.float32(am)
+                if abs(float(n) - t) <= rel * abs(t):
+                    pairs.append((am, w))
+    return pairs
+
+
+def test_quotients_next_to_thresholds():
+    """Blocks whose elements divide to within 2^-12 of a decision midpoint (the
+    closest bf16 quotient lies 1.2e-6 from one): the quantizer's fast grid
+    path and its exact fallback must both agree with the oracle."""
+    pairs = _near_threshold_pairs(2.0 ** -12)
+    assert len(pairs) > 100
+    by_am = {}
+    for a, w in pairs:
+        by_am.setdefault(float(a), []).append(float(w))
+    blocks = []
+    for a, ws in by_am.items():
+        vals = ws + [-w for w in ws]
+        for i in range(0, len(vals), 63):
+            blk = np.zeros(64, np.float32)
+            blk[0] = a                                  # the block absmax
+            chunk = vals[i:i + 63]
+            blk[1:1 + len(chunk)] = chunk
+            blocks.append(blk)
+    t = torch.from_numpy(np.concatenate(blocks)).to(torch.bfloat16)
+    assert np.array_equal(t.float().numpy(), np.concatenate(blocks))   # every value is a bf16
+    p, a = check_quant_exact(t.view(torch.int16).numpy().view(np.uint16))
+    check_dequant_exact(p, a, t.numel())
