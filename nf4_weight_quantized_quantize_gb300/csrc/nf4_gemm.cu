@@ -47,23 +47,22 @@ namespace nf4 {
 constexpr int kBK = 64;                    // K per slice = one NF4 block = one 128-byte activation row
 constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per slice
 
-// Barriers, in shared memory:
-//   full[s1]  TMA landed (activations + packed weights of a K-slice) and the
-//             slice's scales were copied
-//   empty[s1] the MMA of that K-slice completed: its ring slot may be refilled
-//   conv[s2]  a converter group finished writing a TMEM weight slot
-//   cfree[s2] the MMA reading that TMEM slot completed
-//   accum     the accumulator is final; drain: used only on the error path
+// Barriers, in shared memory, one set per stage slot s (a stage is KS
+// consecutive K-slices):
+//   full[s]  the stage's TMA loads landed and its block scales were copied
+//   conv[s]  the converter warps wrote the stage's weights into TMEM slot s
+//   done[s]  the stage's MMAs completed: shared-memory slot s and TMEM slot s
+//            may be reused
+// plus accum (the accumulator is final) and drain (error path only).
 struct Barriers {
     uint32_t base;
-    int s1, s2;
+    int n;
     __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t empty(int s) const { return base + 8u * (s1 + s); }
-    __device__ uint32_t conv(int b) const { return base + 8u * (2 * s1 + b); }
-    __device__ uint32_t cfree(int b) const { return base + 8u * (2 * s1 + s2 + b); }
-    __device__ uint32_t accum() const { return base + 8u * (2 * s1 + 2 * s2); }
-    __device__ uint32_t drain() const { return base + 8u * (2 * s1 + 2 * s2 + 1); }
-    __host__ __device__ static constexpr int count(int a, int b) { return 2 * a + 2 * b + 2; }
+    __device__ uint32_t conv(int s) const { return base + 8u * (n + s); }
+    __device__ uint32_t done(int s) const { return base + 8u * (2 * n + s); }
+    __device__ uint32_t accum() const { return base + 8u * (3 * n); }
+    __device__ uint32_t drain() const { return base + 8u * (3 * n + 1); }
+    __host__ __device__ static constexpr int count(int slots) { return 3 * slots + 2; }
 };
 
 // full[s] completes on the TMA bytes plus kFullArrivals arrivals: the
@@ -71,13 +70,10 @@ struct Barriers {
 constexpr int kFullArrivals = 1 + 32;
 
 __device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arrivals) {
-    for (int s = 0; s < bar.s1; ++s) {
+    for (int s = 0; s < bar.n; ++s) {
         mbar_init(bar.full(s), kFullArrivals);
-        mbar_init(bar.empty(s), 1);
-    }
-    for (int b = 0; b < bar.s2; ++b) {
-        mbar_init(bar.conv(b), conv_arrivals);
-        mbar_init(bar.cfree(b), 1);
+        mbar_init(bar.conv(s), conv_arrivals);
+        mbar_init(bar.done(s), 1);
     }
     mbar_init(bar.accum(), 1);
     mbar_init(bar.drain(), 1);
@@ -145,26 +141,26 @@ __device__ __forceinline__ void expand8(uint32_t p, const CodebookRegs& cb, uint
     o[3] = bf16x2_mul(prmt(lo, hi, 0x6273u), am2);
 }
 
-// Whether a converter warp reports K-slice kb as converted.  Always true in
+// Whether a converter warp reports stage st as converted.  Always true in
 // the library.  A test build (-DNF4_TEST_DROP_CONVERTED_ARRIVE) withholds the
-// report for slice 0 -- a flag that nothing sets -- so the MMA issuer's bounded
+// report for stage 0 -- a flag that nothing sets -- so the MMA issuer's bounded
 // wait runs out and the timeout path (error word, drain, TMEM release, early
 // exit) can be checked on a GPU without faulting or hanging it.
-__device__ __forceinline__ bool report_converted(int kb) {
+__device__ __forceinline__ bool report_converted(int st) {
 #ifdef NF4_TEST_DROP_CONVERTED_ARRIVE
-    return kb != 0;
+    return st != 0;
 #else
-    (void)kb;
+    (void)st;
     return true;
 #endif
 }
 
-// Wait (bounded) for the copies a producer issued into the last `s1`
-// K-slices to land, so no TMA or cp.async write targets shared memory after exit.
+// Wait (bounded) for the copies a producer issued into the last `n` stages
+// to land, so no TMA or cp.async write targets shared memory after exit.
 __device__ __forceinline__ void drain_tma(const Barriers& bar, int issued, uint32_t* err) {
     int dummy = 0;   // a fresh flag: the CTA-wide abort is already raised here
-    for (int kb = max(0, issued - bar.s1); kb < issued; ++kb)
-        if (!mbar_wait(bar.full(kb % bar.s1), (kb / bar.s1) & 1, err, &dummy, kErrTimeoutDrain)) break;
+    for (int st = max(0, issued - bar.n); st < issued; ++st)
+        if (!mbar_wait(bar.full(st % bar.n), (st / bar.n) & 1, err, &dummy, kErrTimeoutDrain)) break;
 }
 
 // Error-path exit of the MMA issuer: wait (bounded) until every MMA it issued
@@ -175,62 +171,74 @@ __device__ __forceinline__ void drain_mma(const Barriers& bar, uint32_t* err) {
     mbar_wait(bar.drain(), 0, err, &dummy, kErrTimeoutDrain);
 }
 
-// Producer warp, one K-slice: lane 0 arms full[s] with the TMA byte count and
-// issues the two tile loads; every lane copies the scales of rows
-// lane, lane + 32, ... of the slice into `am_dst` with 4-byte cp.async and
-// arrives on full[s] when its copies land.  Rows past N copy a harmless
-// in-range scale (their outputs are never stored).
-template <int ROWS>
-__device__ __forceinline__ void produce_slice(const Barriers& bar, int s, int lane, uint32_t tx_bytes,
-                                              const CUtensorMap* tm_x, uint32_t x_dst, int x_col, int x_row,
-                                              const CUtensorMap* tm_w, uint32_t p_dst, int p_col, int n0,
-                                              uint32_t am_dst, const float* absmax, int N, int64_t am_pitch,
-                                              int kb_abs) {
+// Producer warp, one stage of KS K-slices: lane 0 arms full[s] with the TMA
+// byte count and issues KS activation-tile loads (one 128-byte-swizzled
+// [rows, 64] box per K-slice) and one packed-weight load covering the whole
+// stage; every lane copies scales with 4-byte cp.async -- K-slice h, rows
+// lane, lane + 32, ... to am_dst[h][row] -- and arrives on full[s] when its
+// copies land.  Rows past N and K-slices past the weight's last block copy a
+// harmless in-range scale (their products are never stored or multiply zeros).
+template <int ROWS, int KS>
+__device__ __forceinline__ void produce_stage(const Barriers& bar, int s, int lane, uint32_t tx_bytes,
+                                              const CUtensorMap* tm_x, uint32_t x_dst, uint32_t x_bytes,
+                                              int x_col0, int x_row, const CUtensorMap* tm_w, uint32_t p_dst,
+                                              int p_col0, int n0, uint32_t am_dst, const float* absmax, int N,
+                                              int am_pitch, int kb_abs0) {
     if (lane == 0) {
         mbar_arrive_expect_tx(bar.full(s), tx_bytes);
-        tma_load_2d(x_dst, tm_x, bar.full(s), x_col, x_row);
-        tma_load_2d(p_dst, tm_w, bar.full(s), p_col, n0);
+#pragma unroll
+        for (int h = 0; h < KS; ++h)
+            tma_load_2d(x_dst + h * x_bytes, tm_x, bar.full(s), x_col0 + h * kBK, x_row);
+        tma_load_2d(p_dst, tm_w, bar.full(s), p_col0, n0);
     }
 #pragma unroll
-    for (int i = lane; i < ROWS; i += 32) {
-        const int n = n0 + i;
-        const float* src = absmax + (n < N ? static_cast<int64_t>(n) * am_pitch + kb_abs : 0);
-        cp_async_4(am_dst + 4u * i, src);
+    for (int h = 0; h < KS; ++h) {
+        const bool kb_ok = kb_abs0 + h < am_pitch;
+#pragma unroll
+        for (int i = lane; i < ROWS; i += 32) {
+            const int n = n0 + i;
+            const float* src = absmax + (n < N && kb_ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0);
+            cp_async_4(am_dst + 4u * (h * ROWS + i), src);
+        }
     }
     cp_async_arrive_noinc(bar.full(s));
 }
 
 // ============================================================ the kernel
 
-namespace ts {
-constexpr int BW = 128;                      // weight rows per tile (MMA M)
-constexpr int SA = 8;                        // TMEM slots for converted weight K-slices
-constexpr int TMEM_COLS = 512;
-constexpr int A_COL0 = 256;                  // accumulator in columns [0, 256), weight slots above
-constexpr int A_SLOT_COLS = kBK / 2;         // 64 bf16 per row = 32 columns
-constexpr int P_BYTES = BW * kPackedRow;     // 4 KB
-constexpr int AM_BYTES = BW * 4;             // 512 B
-constexpr int SMEM_LIMIT = 232448;
-static_assert(A_COL0 + SA * A_SLOT_COLS <= TMEM_COLS, "TMEM budget");
-__host__ __device__ constexpr int x_bytes(int nx) { return nx * kBK * 2; }
-__host__ __device__ constexpr int slot_bytes(int nx) { return x_bytes(nx) + P_BYTES + AM_BYTES; }
-__host__ __device__ constexpr int stages(int nx) {
-    return (SMEM_LIMIT - 2048) / slot_bytes(nx) > 12 ? 12 : (SMEM_LIMIT - 2048) / slot_bytes(nx);
-}
-__host__ __device__ constexpr int off_p(int nx) { return stages(nx) * x_bytes(nx); }
-__host__ __device__ constexpr int off_am(int nx) { return off_p(nx) + stages(nx) * P_BYTES; }
-__host__ __device__ constexpr int off_bar(int nx) { return off_am(nx) + stages(nx) * AM_BYTES; }
-// At least 120 KB, so no two CTAs share an SM: a second CTA there would wait
-// in tcgen05.alloc for the first one's 512 TMEM columns while another SM idles.
-constexpr size_t MIN_SMEM = 120 * 1024;
-__host__ __device__ constexpr size_t smem_bytes(int nx) {
-    return 1024 + off_bar(nx) + Barriers::count(stages(nx), SA) * 8 + 16 > MIN_SMEM
-               ? 1024 + off_bar(nx) + Barriers::count(stages(nx), SA) * 8 + 16
-               : MIN_SMEM;
-}
-__host__ __device__ constexpr int threads(int groups) { return 64 + groups * 128; }
-static_assert(smem_bytes(256) <= SMEM_LIMIT && smem_bytes(16) <= SMEM_LIMIT, "shared memory budget");
-}  // namespace ts
+// Compile-time layout of one kernel instance: NX activation rows per tile
+// (MMA N), stages of KS K-slices.
+template <int NX, int KS>
+struct TsCfg {
+    static constexpr int BW = 128;                      // weight rows per tile (MMA M)
+    static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
+    static constexpr int P_BYTES = BW * kPackedRow * KS;
+    static constexpr int AM_BYTES = BW * 4 * KS;
+    static constexpr int SLOT_BYTES = KS * XB + P_BYTES + AM_BYTES;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int A_COL0 = NX <= 32 ? 32 : (NX + 31) / 32 * 32;   // accumulator in [0, NX)
+    static constexpr int A_SLOT = 32 * KS;              // 64 bf16 per row per K-slice = 32 columns
+    static constexpr int TMEM_SLOTS = (TMEM_COLS - A_COL0) / A_SLOT;
+    static constexpr int SMEM_LIMIT = 232448;
+    static constexpr int SMEM_SLOTS = (SMEM_LIMIT - 2048) / SLOT_BYTES;
+    static constexpr int S = TMEM_SLOTS < SMEM_SLOTS ? (TMEM_SLOTS < 8 ? TMEM_SLOTS : 8)
+                                                     : (SMEM_SLOTS < 8 ? SMEM_SLOTS : 8);
+    static constexpr int OFF_P = S * KS * XB;
+    static constexpr int OFF_AM = OFF_P + S * P_BYTES;
+    static constexpr int OFF_BAR = OFF_AM + S * AM_BYTES;
+    // At least 120 KB, so no two CTAs share an SM: a second CTA there would
+    // wait in tcgen05.alloc for the first one's 512 TMEM columns while
+    // another SM idles.
+    static constexpr size_t USED = 1024 + OFF_BAR + Barriers::count(S) * 8 + 16;
+    static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+    static constexpr int CONV_WARPS = 4 * KS;           // warp (4h + q): K-slice h, TMEM lane quarter q
+    static constexpr int THREADS = 64 + 32 * CONV_WARPS;
+    static_assert(NX % 16 == 0 && NX >= 16 && NX <= 256, "MMA N");
+    static_assert(XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
+    static_assert(S >= 2, "at least two stages");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
+    static_assert(32 * KS <= 256, "packed-weight box width");
+};
 
 struct TsArgs {
     const float* absmax;  // [N, K/64]
@@ -242,40 +250,36 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int G, bool SPLIT>
-__global__ void __launch_bounds__(ts::threads(G), 1)
+template <int NX, int KS, bool SPLIT>
+__global__ void __launch_bounds__(TsCfg<NX, KS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using namespace ts;
-    constexpr int S = stages(NX);
-    constexpr int XB = x_bytes(NX);
-    constexpr int NUM_BARS = Barriers::count(S, SA);
-    static_assert(NX % 16 == 0 && NX >= 16 && NX <= 256, "MMA N");
-    static_assert(XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
-    static_assert(SA % G == 0, "a TMEM slot always belongs to the same converter group");
+    using C = TsCfg<NX, KS>;
+    constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + off_bar(NX));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + NUM_BARS);
+    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + Barriers::count(S));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const Barriers bar{smem_u32(bar_mem), S, SA};
+    const Barriers bar{smem_u32(bar_mem), S};
 
-    auto x_tile = [&](int s) { return smem + s * XB; };
-    auto p_tile = [&](int s) { return smem + off_p(NX) + s * P_BYTES; };
-    auto am_tile = [&](int s) { return reinterpret_cast<const float*>(smem + off_am(NX) + s * AM_BYTES); };
+    auto x_tile = [&](int s, int h) { return smem + (s * KS + h) * C::XB; };
+    auto p_tile = [&](int s) { return smem + C::OFF_P + s * C::P_BYTES; };
+    auto am_tile = [&](int s) { return reinterpret_cast<const float*>(smem + C::OFF_AM + s * C::AM_BYTES); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // tiles run m-fastest: CTAs resident together share each weight tile through L2
     const int m0 = static_cast<int>(blockIdx.x % args.m_tiles) * NX;
-    const int n0 = static_cast<int>(blockIdx.x / args.m_tiles) * BW;
+    const int n0 = static_cast<int>(blockIdx.x / args.m_tiles) * C::BW;
     const int split = blockIdx.y;
     const int nk_total = args.K / kBK;
     const int kb0 = split * args.kb_per_split;
     const int nk = min(args.kb_per_split, nk_total - kb0);
+    const int nst = (nk + KS - 1) / KS;   // stages; the last may hold fewer than KS K-slices
 
     if (threadIdx.x == 0) {
-        init_barriers(bar, 4);
+        init_barriers(bar, C::CONV_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -284,7 +288,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         tma_prefetch_desc(&tm_w);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -295,37 +299,43 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     if (warp == 0) {
         // ---------------- producer warp
         int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % S;
+        for (int st = 0; st < nst; ++st) {
+            const int s = st % S;
             bool ok = true;
-            if (kb >= S) ok = mbar_wait(bar.empty(s), ((kb / S) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (st >= S) ok = mbar_wait(bar.done(s), ((st / S) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
-            produce_slice<BW>(bar, s, lane, XB + P_BYTES, &tm_x, smem_u32(x_tile(s)), (kb0 + kb) * kBK, m0, &tm_w,
-                              smem_u32(p_tile(s)), (kb0 + kb) * kPackedRow, n0, smem_u32(am_tile(s)), args.absmax,
-                              args.N, nk_total, kb0 + kb);
+            const int kb = kb0 + st * KS;
+            produce_stage<C::BW, KS>(bar, s, lane, KS * C::XB + C::P_BYTES, &tm_x, smem_u32(x_tile(s, 0)), C::XB,
+                                     kb * kBK, m0, &tm_w, smem_u32(p_tile(s)), kb * kPackedRow, n0,
+                                     smem_u32(am_tile(s)), args.absmax, args.N, nk_total, kb);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_tma(bar, issued, args.err);
     } else if (warp == 1) {
-        // ---------------- MMA issuer.  A converter group arrives on conv only
-        // after it has observed full[s], so conv also orders the TMA's
-        // activation tile before the MMA.
+        // ---------------- MMA issuer: one wait, one fence and one commit per
+        // stage.  The converters arrive on conv only after observing full[s],
+        // so conv also orders the TMA's activation tiles before the MMAs.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, NX);
             bool ok = true;
-            for (int kb = 0; kb < nk && ok; ++kb) {
-                const int s = kb % S;
-                const int a = kb % SA;
-                ok = mbar_wait(bar.conv(a), (kb / SA) & 1, args.err, abort_flag, kErrTimeoutConverted);
+            for (int st = 0; st < nst && ok; ++st) {
+                const int s = st % S;
+                ok = mbar_wait(bar.conv(s), (st / S) & 1, args.err, abort_flag, kErrTimeoutConverted);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a_col = tmem + A_COL0 + a * A_SLOT_COLS;
-                const uint32_t x0 = smem_u32(x_tile(s));
+                const int kbs = min(KS, nk - st * KS);
+                const uint32_t a_col = tmem + C::A_COL0 + s * C::A_SLOT;
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)
-                    mma_bf16_ts(tmem, a_col + 8 * j, smem_desc_sw128(x0 + 32 * j), idesc, (kb > 0 || j > 0) ? 1u : 0u);
-                mma_commit(bar.empty(s));
-                mma_commit(bar.cfree(a));
+                for (int h = 0; h < KS; ++h) {
+                    if (h < kbs) {
+                        const uint32_t x0 = smem_u32(x_tile(s, h));
+#pragma unroll
+                        for (int j = 0; j < kBK / 16; ++j)
+                            mma_bf16_ts(tmem, a_col + 32 * h + 8 * j, smem_desc_sw128(x0 + 32 * j), idesc,
+                                        (st > 0 || h > 0 || j > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar.done(s));
             }
             if (ok)
                 mma_commit(bar.accum());
@@ -333,52 +343,56 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 drain_mma(bar, args.err);
         }
     } else {
-        // ---------------- converter groups (one thread per weight row), then epilogue
-        const int g = (warp - 2) >> 2;           // converter group
+        // ---------------- converters: warp 2 + 4h + q converts K-slice h of each
+        // stage for TMEM lane quarter q (one thread per weight row); then epilogue
+        const int cw = warp - 2;
+        const int h = cw >> 2;                   // K-slice within the stage
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;             // weight row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const CodebookRegs cb = codebook_regs();
         bool ok = true;
-        for (int kb = g; kb < nk; kb += G) {
-            const int s = kb % S;
-            const int a = kb % SA;
-            // every lane polls; the outcome is made warp-uniform before anyone branches
-            bool got = mbar_wait(bar.full(s), (kb / S) & 1, args.err, abort_flag, kErrTimeoutFull);
-            if (got && kb >= SA)
-                got = mbar_wait(bar.cfree(a), ((kb / SA) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+        for (int st = 0; st < nst; ++st) {
+            const int s = st % S;
+            // Observing full[s] also orders this stage after the MMAs that last
+            // read TMEM slot s: the producer refilled slot s only after done[s].
+            const bool got = mbar_wait(bar.full(s), (st / S) & 1, args.err, abort_flag, kErrTimeoutFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
-            const float am = am_tile(s)[r];
-            const uint32_t am2 = pack_bf16x2(am, am);
-            const uint4 q0 = *reinterpret_cast<const uint4*>(p_tile(s) + r * kPackedRow);
-            const uint4 q1 = *reinterpret_cast<const uint4*>(p_tile(s) + r * kPackedRow + 16);
-            uint32_t v[32];
-            expand8(q0.x, cb, am2, v + 0);
-            expand8(q0.y, cb, am2, v + 4);
-            expand8(q0.z, cb, am2, v + 8);
-            expand8(q0.w, cb, am2, v + 12);
-            expand8(q1.x, cb, am2, v + 16);
-            expand8(q1.y, cb, am2, v + 20);
-            expand8(q1.z, cb, am2, v + 24);
-            expand8(q1.w, cb, am2, v + 28);
-            tmem_st32(lane_addr + A_COL0 + a * A_SLOT_COLS, v);
-            tmem_st_wait();
+            tc_fence_after();
+            if (st * KS + h < nk) {
+                const float am = am_tile(s)[h * C::BW + r];
+                const uint32_t am2 = pack_bf16x2(am, am);
+                const uint8_t* prow = p_tile(s) + r * (kPackedRow * KS) + kPackedRow * h;
+                const uint4 q0 = *reinterpret_cast<const uint4*>(prow);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(prow + 16);
+                uint32_t v[32];
+                expand8(q0.x, cb, am2, v + 0);
+                expand8(q0.y, cb, am2, v + 4);
+                expand8(q0.z, cb, am2, v + 8);
+                expand8(q0.w, cb, am2, v + 12);
+                expand8(q1.x, cb, am2, v + 16);
+                expand8(q1.y, cb, am2, v + 20);
+                expand8(q1.z, cb, am2, v + 24);
+                expand8(q1.w, cb, am2, v + 28);
+                tmem_st32(lane_addr + C::A_COL0 + s * C::A_SLOT + 32 * h, v);
+                tmem_st_wait();
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && report_converted(kb)) mbar_arrive(bar.conv(a));
+            if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(s));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             // accumulator: TMEM lane = weight row n, column c = activation row m0 + c;
-            // 16-column chunks go round-robin over the converter groups
+            // 16-column chunks go round-robin over the KS warps of each lane quarter
             const int n = n0 + r;
 #pragma unroll 1
-            for (int c0 = 16 * g; c0 < NX; c0 += 16 * G) {
+            for (int c0 = 16 * h; c0 < NX; c0 += 16 * KS) {
                 uint32_t v[16];
                 tmem_ld16(lane_addr + c0, v);
                 tmem_ld_wait();
@@ -404,7 +418,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -424,8 +438,15 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
 namespace {
 
 constexpr int kTargetCtas = 152;             // one wave on a GB300 (152 SMs)
-constexpr int kGroupsDirect = 2;
-constexpr int kGroupsSplit = 4;
+#ifndef NF4_KS_DIRECT
+#define NF4_KS_DIRECT 2
+#endif
+#ifndef NF4_KS_SPLIT
+#define NF4_KS_SPLIT 4
+#endif
+constexpr int kBW = 128;                     // weight rows per tile
+constexpr int kKsDirect = NF4_KS_DIRECT;     // K-slices per stage, M >= 128
+constexpr int kKsSplit = NF4_KS_SPLIT;       // K-slices per stage, M < 128
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -489,7 +510,7 @@ struct Plan {
 Plan make_plan(int64_t M, int64_t N, int64_t K) {
     Plan p;
     const int nk = static_cast<int>(K / kBK);
-    p.n_tiles = static_cast<int>((N + ts::BW - 1) / ts::BW);
+    p.n_tiles = static_cast<int>((N + kBW - 1) / kBW);
     if (M >= 128) {
         p.split = false;
         p.m_tiles = static_cast<int>((M + 255) / 256);
@@ -503,53 +524,55 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
         p.nx = static_cast<int>(((M + 15) / 16) * 16);
         int splits = std::max(1, kTargetCtas / std::max(1, p.n_tiles));
         splits = std::min(splits, nk);
-        p.kb_per_split = (nk + splits - 1) / splits;
-        p.splits = (nk + p.kb_per_split - 1) / p.kb_per_split;   // no empty split
+        const int per = (nk + splits - 1) / splits;
+        p.kb_per_split = (per + kKsSplit - 1) / kKsSplit * kKsSplit;   // whole stages
+        p.splits = (nk + p.kb_per_split - 1) / p.kb_per_split;          // no empty split
     }
     return p;
 }
 
-template <int NX, int G, bool SPLIT>
+template <int NX, int KS, bool SPLIT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    constexpr size_t smem = ts::smem_bytes(NX);
-    if (dev.smem_optin < smem) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, G, SPLIT>;
-    if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), smem, dev.ordinal); e != cudaSuccess) return e;
+    using C = TsCfg<NX, KS>;
+    if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
+    auto kernel = ts_kernel<NX, KS, SPLIT>;
+    if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
+        return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > 0x7fffffff || p.splits > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits));
-    kernel<<<grid, ts::threads(G), smem, s>>>(tm_x, tm_w, a);
+    kernel<<<grid, C::THREADS, C::SMEM, s>>>(tm_x, tm_w, a);
     count_launches(1);
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int G>
+template <bool SPLIT, int KS>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, G, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -560,12 +583,13 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
                         cudaStream_t s) {
     CUtensorMap tm_x, tm_w;
     if (!make_map(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, p.nx, kBK, true) ||
-        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, ts::BW, kPackedRow, false))
+        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, kBW,
+                  kPackedRow * (p.split ? kKsSplit : kKsDirect), false))
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
              p.m_tiles, dev.err_word};
-    return p.split ? dispatch_nx<true, kGroupsSplit>(dev, p, tm_x, tm_w, a, s)
-                   : dispatch_nx<false, kGroupsDirect>(dev, p, tm_x, tm_w, a, s);
+    return p.split ? dispatch_nx<true, kKsSplit>(dev, p, tm_x, tm_w, a, s)
+                   : dispatch_nx<false, kKsDirect>(dev, p, tm_x, tm_w, a, s);
 }
 
 }  // namespace
