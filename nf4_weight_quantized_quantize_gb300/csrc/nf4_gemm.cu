@@ -25,11 +25,11 @@
 // Warp roles: warp 0 is the producer (lane 0 issues the TMA loads of the
 // activation and packed-weight tiles, all lanes copy the block scales with
 // cp.async); warp 1 allocates TMEM and lane 0 issues the MMAs; the remaining
-// warps form G converter groups of 4 warps (one thread per weight row) that
-// take K-slices round-robin, so one group's barrier waits overlap another's
-// work.  A converter looks each 4-bit code up in a 16-entry bf16 codebook held
-// in registers (byte permutes), scales it by the block absmax with one bf16x2
-// multiply, and stores its row's 64 values into its TMEM lane with
+// warps are converters, 4 x KS x RS of them: each K-slice of a stage has RS
+// groups of 4 warps (one thread per weight row, each taking 64 / RS of the
+// row's values).  A converter looks each 4-bit code up in a 16-entry bf16
+// codebook held in registers (byte permutes), scales it by the block absmax
+// with one bf16x2 multiply, and stores the values into its TMEM lane with
 // tcgen05.st.  Every wait is bounded (NF4_WAIT_LIMIT_NS); on expiry the CTA
 // records an error code, drains what it has in flight and returns.
 #include <algorithm>
@@ -207,8 +207,9 @@ __device__ __forceinline__ void produce_stage(const Barriers& bar, int s, int la
 // ============================================================ the kernel
 
 // Compile-time layout of one kernel instance: NX activation rows per tile
-// (MMA N), stages of KS K-slices.
-template <int NX, int KS>
+// (MMA N), stages of KS K-slices, RS converter threads per weight row and
+// K-slice (each expands 64 / RS of the row's values).
+template <int NX, int KS, int RS>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
     static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
@@ -231,13 +232,15 @@ struct TsCfg {
     // another SM idles.
     static constexpr size_t USED = 1024 + OFF_BAR + Barriers::count(S) * 8 + 16;
     static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
-    static constexpr int CONV_WARPS = 4 * KS;           // warp (4h + q): K-slice h, TMEM lane quarter q
+    static constexpr int CONV_WARPS = 4 * KS * RS;      // warp 2 + 4u + q: unit u, TMEM lane quarter q
     static constexpr int THREADS = 64 + 32 * CONV_WARPS;
     static_assert(NX % 16 == 0 && NX >= 16 && NX <= 256, "MMA N");
     static_assert(XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
     static_assert(S >= 2, "at least two stages");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
     static_assert(32 * KS <= 256, "packed-weight box width");
+    static_assert(RS == 1 || RS == 2, "converter threads per row");
+    static_assert(THREADS <= 1024, "block size");
 };
 
 struct TsArgs {
@@ -250,11 +253,11 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int KS, bool SPLIT>
-__global__ void __launch_bounds__(TsCfg<NX, KS>::THREADS, 1)
+template <int NX, int KS, int RS, bool SPLIT>
+__global__ void __launch_bounds__(TsCfg<NX, KS, RS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using C = TsCfg<NX, KS>;
+    using C = TsCfg<NX, KS, RS>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -343,10 +346,12 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 drain_mma(bar, args.err);
         }
     } else {
-        // ---------------- converters: warp 2 + 4h + q converts K-slice h of each
-        // stage for TMEM lane quarter q (one thread per weight row); then epilogue
-        const int cw = warp - 2;
-        const int h = cw >> 2;                   // K-slice within the stage
+        // ---------------- converters: unit u = (warp - 2) / 4 converts part
+        // u / KS (of RS) of K-slice u % KS of each stage for TMEM lane quarter
+        // q = warp % 4 (one thread per weight row and part); then epilogue
+        const int u = (warp - 2) >> 2;
+        const int h = u % KS;                    // K-slice within the stage
+        const int part = u / KS;                 // which 64 / RS values of the row
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;             // weight row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -366,18 +371,30 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 const float am = am_tile(s)[h * C::BW + r];
                 const uint32_t am2 = pack_bf16x2(am, am);
                 const uint8_t* prow = p_tile(s) + r * (kPackedRow * KS) + kPackedRow * h;
-                const uint4 q0 = *reinterpret_cast<const uint4*>(prow);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(prow + 16);
-                uint32_t v[32];
-                expand8(q0.x, cb, am2, v + 0);
-                expand8(q0.y, cb, am2, v + 4);
-                expand8(q0.z, cb, am2, v + 8);
-                expand8(q0.w, cb, am2, v + 12);
-                expand8(q1.x, cb, am2, v + 16);
-                expand8(q1.y, cb, am2, v + 20);
-                expand8(q1.z, cb, am2, v + 24);
-                expand8(q1.w, cb, am2, v + 28);
-                tmem_st32(lane_addr + C::A_COL0 + s * C::A_SLOT + 32 * h, v);
+                const uint32_t col = lane_addr + C::A_COL0 + s * C::A_SLOT + 32 * h;
+                if constexpr (RS == 1) {
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(prow);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(prow + 16);
+                    uint32_t v[32];
+                    expand8(q0.x, cb, am2, v + 0);
+                    expand8(q0.y, cb, am2, v + 4);
+                    expand8(q0.z, cb, am2, v + 8);
+                    expand8(q0.w, cb, am2, v + 12);
+                    expand8(q1.x, cb, am2, v + 16);
+                    expand8(q1.y, cb, am2, v + 20);
+                    expand8(q1.z, cb, am2, v + 24);
+                    expand8(q1.w, cb, am2, v + 28);
+                    tmem_st32(col, v);
+                } else {
+                    // 16 packed bytes = 32 values = 16 TMEM columns
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(prow + 16 * part);
+                    uint32_t v[16];
+                    expand8(q0.x, cb, am2, v + 0);
+                    expand8(q0.y, cb, am2, v + 4);
+                    expand8(q0.z, cb, am2, v + 8);
+                    expand8(q0.w, cb, am2, v + 12);
+                    tmem_st16(col + 16 * part, v);
+                }
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -389,10 +406,10 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             // accumulator: TMEM lane = weight row n, column c = activation row m0 + c;
-            // 16-column chunks go round-robin over the KS warps of each lane quarter
+            // 16-column chunks go round-robin over the KS * RS warps of each lane quarter
             const int n = n0 + r;
 #pragma unroll 1
-            for (int c0 = 16 * h; c0 < NX; c0 += 16 * KS) {
+            for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
                 uint32_t v[16];
                 tmem_ld16(lane_addr + c0, v);
                 tmem_ld_wait();
@@ -444,9 +461,14 @@ constexpr int kTargetCtas = 152;             // one wave on a GB300 (152 SMs)
 #ifndef NF4_KS_SPLIT
 #define NF4_KS_SPLIT 4
 #endif
+#ifndef NF4_RS_DIRECT
+#define NF4_RS_DIRECT 2
+#endif
 constexpr int kBW = 128;                     // weight rows per tile
 constexpr int kKsDirect = NF4_KS_DIRECT;     // K-slices per stage, M >= 128
 constexpr int kKsSplit = NF4_KS_SPLIT;       // K-slices per stage, M < 128
+constexpr int kRsDirect = NF4_RS_DIRECT;     // converter threads per weight row, M >= 128
+constexpr int kRsSplit = 1;                  // converter threads per weight row, M < 128
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -531,12 +553,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, bool SPLIT>
+template <int NX, int KS, int RS, bool SPLIT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    using C = TsCfg<NX, KS>;
+    using C = TsCfg<NX, KS, RS>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, SPLIT>;
+    auto kernel = ts_kernel<NX, KS, RS, SPLIT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -547,32 +569,32 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS>
+template <bool SPLIT, int KS, int RS>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -588,8 +610,8 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
              p.m_tiles, dev.err_word};
-    return p.split ? dispatch_nx<true, kKsSplit>(dev, p, tm_x, tm_w, a, s)
-                   : dispatch_nx<false, kKsDirect>(dev, p, tm_x, tm_w, a, s);
+    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit>(dev, p, tm_x, tm_w, a, s)
+                   : dispatch_nx<false, kKsDirect, kRsDirect>(dev, p, tm_x, tm_w, a, s);
 }
 
 }  // namespace

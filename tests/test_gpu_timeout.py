@@ -45,7 +45,7 @@ def _inputs(m, n, k, seed):
     return x.to(DEV), torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV), workloads.bits(x), p, a
 
 
-@pytest.mark.parametrize("m", [256, 16], ids=["tile_kernel", "skinny_kernel"])
+@pytest.mark.parametrize("m", [256, 64], ids=["tile_kernel", "split_kernel"])
 def test_bounded_wait_expires_and_reports(faulty_lib, m):
     n, k = 512, 1024
     x, pd, ad, _, _, _ = _inputs(m, n, k, m)
