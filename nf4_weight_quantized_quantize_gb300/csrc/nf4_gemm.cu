@@ -240,6 +240,17 @@ struct TsCfg {
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
     static_assert(32 * KS <= 256, "packed-weight box width");
     static_assert(RS == 1 || RS == 2, "converter threads per row");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "packed rows of 32, 64 or 128 bytes");
+    // The packed tile is loaded with the TMA swizzle whose span equals its
+    // row (32 * KS bytes): 16-byte chunk c of row r lands at chunk
+    // c ^ ((r * 32 * KS / 128) mod 32 * KS / 16).  A converter warp reads
+    // one chunk from each of 32 consecutive rows; the swizzle spreads them
+    // over all 32 banks, where plain rows would put them on the same four.
+    static constexpr uint32_t SWZ_MASK = 2 * KS - 1;
+    __device__ static uint32_t packed_offset(int row, int chunk) {
+        const uint32_t o = static_cast<uint32_t>(row * kPackedRow * KS + 16 * chunk);
+        return o ^ (((o >> 7) & SWZ_MASK) << 4);
+    }
     static_assert(THREADS <= 1024, "block size");
 };
 
@@ -370,11 +381,11 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (st * KS + h < nk) {
                 const float am = am_tile(s)[h * C::BW + r];
                 const uint32_t am2 = pack_bf16x2(am, am);
-                const uint8_t* prow = p_tile(s) + r * (kPackedRow * KS) + kPackedRow * h;
+                const uint8_t* ptile = p_tile(s);
                 const uint32_t col = lane_addr + C::A_COL0 + s * C::A_SLOT + 32 * h;
                 if constexpr (RS == 1) {
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(prow);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(prow + 16);
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h));
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + 1));
                     uint32_t v[32];
                     expand8(q0.x, cb, am2, v + 0);
                     expand8(q0.y, cb, am2, v + 4);
@@ -387,7 +398,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     tmem_st32(col, v);
                 } else {
                     // 16 packed bytes = 32 values = 16 TMEM columns
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(prow + 16 * part);
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + part));
                     uint32_t v[16];
                     expand8(q0.x, cb, am2, v + 0);
                     expand8(q0.y, cb, am2, v + 4);
@@ -487,9 +498,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D row-major tensor [rows, cols] of `elem` bytes per element, box
-// {box_cols, box_rows}, optional 128-byte swizzle; out-of-range reads fill 0.
+// {box_cols, box_rows}, the given shared-memory swizzle; out-of-range reads fill 0.
 bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem, uint64_t rows,
-              uint64_t cols, uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
+              uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -497,7 +508,7 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    swizzle,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -604,9 +615,13 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
                         const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, float* ws,
                         cudaStream_t s) {
     CUtensorMap tm_x, tm_w;
-    if (!make_map(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, p.nx, kBK, true) ||
-        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, kBW,
-                  kPackedRow * (p.split ? kKsSplit : kKsDirect), false))
+    const int ks = p.split ? kKsSplit : kKsDirect;
+    // the packed box row is 32 * ks bytes; its swizzle span matches (TsCfg::packed_offset)
+    const CUtensorMapSwizzle wsw = ks == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                 : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, p.nx, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, kBW, kPackedRow * ks, wsw))
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
              p.m_tiles, dev.err_word};

@@ -201,7 +201,11 @@ constexpr int kDequantThreads = 256;
 // outputs, 2 KB).  In step i (0..3) lane t reads packed word 32i + t (one
 // coalesced 128-byte line per warp), looks its 4 bytes up in the 256-entry
 // bf16x2 table, scales by the block absmax and writes one 16-byte word
-// (one coalesced 512-byte line per warp).
+// (one coalesced 512-byte line per warp).  A warp takes kDequantTiles
+// consecutive tiles per iteration, issuing all their loads before the first
+// store, so each warp keeps 1 KB of reads in flight.
+constexpr int kDequantTiles = 2;
+
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict__ absmax,
                    int64_t ntiles, uint4* __restrict__ out) {
@@ -211,22 +215,35 @@ dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict_
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kDequantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kDequantThreads) >> 5;
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
-        uint32_t p[4];
-        float a[4];
+    constexpr int U = kDequantTiles;
+    for (int64_t t0 = warp * U; t0 < ntiles; t0 += nwarps * U) {
+        uint32_t p[4 * U];
+        float a[4 * U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            p[i] = ldg_nc_u32(packed + tile * 128 + 32 * i + lane);
-            a[i] = ldg_nc_f32(absmax + tile * 16 + 4 * i + (lane >> 3));
+        for (int u = 0; u < U; ++u) {
+            const int64_t tile = min(t0 + u, ntiles - 1);   // past the end: reload the last tile, store nothing
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[4 * u + i] = ldg_nc_u32(packed + tile * 128 + 32 * i + lane);
+                a[4 * u + i] = ldg_nc_f32(absmax + tile * 16 + 4 * i + (lane >> 3));
+            }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 o;
-            o.x = scale_entry(lut[p[i] & 0xffu], a[i]);
-            o.y = scale_entry(lut[(p[i] >> 8) & 0xffu], a[i]);
-            o.z = scale_entry(lut[(p[i] >> 16) & 0xffu], a[i]);
-            o.w = scale_entry(lut[p[i] >> 24], a[i]);
-            stg_v4(out + tile * 128 + 32 * i + lane, o);
+        for (int u = 0; u < U; ++u) {
+            const int64_t tile = t0 + u;
+            if (tile < ntiles) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t q = p[4 * u + i];
+                    const float am = a[4 * u + i];
+                    uint4 o;
+                    o.x = scale_entry(lut[q & 0xffu], am);
+                    o.y = scale_entry(lut[(q >> 8) & 0xffu], am);
+                    o.z = scale_entry(lut[(q >> 16) & 0xffu], am);
+                    o.w = scale_entry(lut[q >> 24], am);
+                    stg_v4(out + tile * 128 + 32 * i + lane, o);
+                }
+            }
         }
     }
 }
@@ -250,11 +267,12 @@ __global__ void dequant_scalar_kernel(const uint8_t* __restrict__ packed,
 
 // ============================================================ launchers
 
-static int grid_for(const DeviceInfo& dev, const void* kernel, int threads, int64_t work_items) {
+// rounds x (SMs x resident CTAs per SM), capped at the number of work items
+static int grid_for(const DeviceInfo& dev, const void* kernel, int threads, int64_t work_items, int rounds = 1) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
         per_sm = 1;
-    int64_t g = static_cast<int64_t>(dev.sm_count) * per_sm;
+    int64_t g = static_cast<int64_t>(dev.sm_count) * per_sm * rounds;
     if (work_items < g) g = work_items;
     return static_cast<int>(g < 1 ? 1 : g);
 }
@@ -297,8 +315,11 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
     if (aligned) {
         const int64_t ntiles = nbytes / 512;
         if (ntiles > 0) {
-            const int grid = grid_for(dev, reinterpret_cast<const void*>(dequant_vec_kernel),
-                                      kDequantThreads, (ntiles + kDequantThreads / 32 - 1) / (kDequantThreads / 32));
+            // twice the resident CTAs: the second round starts on SMs as
+            // the first one drains, which evens out the end of the grid
+            const int64_t warp_items = (ntiles + kDequantTiles - 1) / kDequantTiles;
+            const int grid = grid_for(dev, reinterpret_cast<const void*>(dequant_vec_kernel), kDequantThreads,
+                                      (warp_items + kDequantThreads / 32 - 1) / (kDequantThreads / 32), 2);
             dequant_vec_kernel<<<grid, kDequantThreads, 0, s>>>(
                 reinterpret_cast<const uint32_t*>(packed), absmax, ntiles, reinterpret_cast<uint4*>(out));
             count_launches(1);
