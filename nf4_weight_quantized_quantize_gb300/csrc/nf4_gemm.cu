@@ -47,36 +47,53 @@ namespace nf4 {
 constexpr int kBK = 64;                    // K per slice = one NF4 block = one 128-byte activation row
 constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per slice
 
-// Barriers, in shared memory, one set per stage slot s (a stage is KS
-// consecutive K-slices):
-//   full[s]  the stage's TMA loads landed and its block scales were copied
-//   conv[s]  the converter warps wrote the stage's weights into TMEM slot s
-//   done[s]  the stage's MMAs completed: shared-memory slot s and TMEM slot s
-//            may be reused
-// plus accum (the accumulator is final) and drain (error path only).
+// Barriers, in shared memory.  A stage is KS consecutive K-slices.  Three
+// rings carry it, each as deep as its storage allows:
+//   TMEM ring (ST slots): the stage's converted weights;
+//   activation ring (SX <= ST slots of shared memory): its activation tiles;
+//   weight ring (SP slots of shared memory): its packed bytes and scales,
+//     free again as soon as the converters have read them.
+// Stage st uses TMEM slot st % ST, activation slot st % SX, weight slot
+// st % SP.
+//   xfull[s]   the stage's activation tiles landed (TMA)
+//   conv[t]    the converter warps wrote the stage's weights into TMEM slot t
+//   done[t]    the stage's MMAs completed (one commit per MMA issuer): TMEM
+//              slot t may be rewritten, and the activation slot of stage st
+//              (st % SX) may be refilled
+//   pfull[p]   the stage's packed tile landed (TMA) and its scales were copied
+//   pempty[p]  every converter warp has read weight slot p
+// plus accum (the accumulators are final) and one drain barrier per MMA
+// issuer (error path only).
 struct Barriers {
     uint32_t base;
-    int n;
-    __device__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ uint32_t conv(int s) const { return base + 8u * (n + s); }
-    __device__ uint32_t done(int s) const { return base + 8u * (2 * n + s); }
-    __device__ uint32_t accum() const { return base + 8u * (3 * n); }
-    __device__ uint32_t drain() const { return base + 8u * (3 * n + 1); }
-    __host__ __device__ static constexpr int count(int slots) { return 3 * slots + 2; }
+    int nx, nt, np;
+    __device__ uint32_t xfull(int s) const { return base + 8u * s; }
+    __device__ uint32_t conv(int t) const { return base + 8u * (nx + t); }
+    __device__ uint32_t done(int t) const { return base + 8u * (nx + nt + t); }
+    __device__ uint32_t pfull(int p) const { return base + 8u * (nx + 2 * nt + p); }
+    __device__ uint32_t pempty(int p) const { return base + 8u * (nx + 2 * nt + np + p); }
+    __device__ uint32_t accum() const { return base + 8u * (nx + 2 * nt + 2 * np); }
+    __device__ uint32_t drain(int issuer) const { return base + 8u * (nx + 2 * nt + 2 * np + 1 + issuer); }
+    __host__ __device__ static constexpr int count(int xs, int ts, int ps) { return xs + 2 * ts + 2 * ps + 3; }
 };
 
-// full[s] completes on the TMA bytes plus kFullArrivals arrivals: the
-// producer lane's expect-tx arrive and one cp.async arrive per producer lane.
-constexpr int kFullArrivals = 1 + 32;
+// pfull[p] completes on the TMA bytes plus kPfullArrivals arrivals: the
+// weight producer lane's expect-tx arrive and one cp.async arrive per lane.
+constexpr int kPfullArrivals = 1 + 32;
 
-__device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arrivals) {
-    for (int s = 0; s < bar.n; ++s) {
-        mbar_init(bar.full(s), kFullArrivals);
-        mbar_init(bar.conv(s), conv_arrivals);
-        mbar_init(bar.done(s), 1);
+__device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arrivals, int mma_issuers) {
+    for (int s = 0; s < bar.nx; ++s) mbar_init(bar.xfull(s), 1);
+    for (int t = 0; t < bar.nt; ++t) {
+        mbar_init(bar.conv(t), conv_arrivals);
+        mbar_init(bar.done(t), mma_issuers);
     }
-    mbar_init(bar.accum(), 1);
-    mbar_init(bar.drain(), 1);
+    for (int p = 0; p < bar.np; ++p) {
+        mbar_init(bar.pfull(p), kPfullArrivals);
+        mbar_init(bar.pempty(p), conv_arrivals);
+    }
+    mbar_init(bar.accum(), mma_issuers);
+    mbar_init(bar.drain(0), 1);
+    mbar_init(bar.drain(1), 1);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -155,41 +172,37 @@ __device__ __forceinline__ bool report_converted(int st) {
 #endif
 }
 
-// Wait (bounded) for the copies a producer issued into the last `n` stages
-// to land, so no TMA or cp.async write targets shared memory after exit.
-__device__ __forceinline__ void drain_tma(const Barriers& bar, int issued, uint32_t* err) {
+// Wait (bounded) for the copies a producer issued into the last `slots`
+// stages of its ring to land, so no TMA or cp.async write targets shared
+// memory after exit.
+__device__ __forceinline__ void drain_ring(uint32_t bar0, int slots, int issued, uint32_t* err) {
     int dummy = 0;   // a fresh flag: the CTA-wide abort is already raised here
-    for (int st = max(0, issued - bar.n); st < issued; ++st)
-        if (!mbar_wait(bar.full(st % bar.n), (st / bar.n) & 1, err, &dummy, kErrTimeoutDrain)) break;
+    for (int st = max(0, issued - slots); st < issued; ++st)
+        if (!mbar_wait(bar0 + 8u * (st % slots), (st / slots) & 1, err, &dummy, kErrTimeoutDrain)) break;
 }
 
-// Error-path exit of the MMA issuer: wait (bounded) until every MMA it issued
+// Error-path exit of an MMA issuer: wait (bounded) until every MMA it issued
 // has completed, so TMEM can be released.
-__device__ __forceinline__ void drain_mma(const Barriers& bar, uint32_t* err) {
+__device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint32_t* err) {
     int dummy = 0;
-    mma_commit(bar.drain());
-    mbar_wait(bar.drain(), 0, err, &dummy, kErrTimeoutDrain);
+    mma_commit(bar.drain(issuer));
+    mbar_wait(bar.drain(issuer), 0, err, &dummy, kErrTimeoutDrain);
 }
 
-// Producer warp, one stage of KS K-slices: lane 0 arms full[s] with the TMA
-// byte count and issues KS activation-tile loads (one 128-byte-swizzled
-// [rows, 64] box per K-slice) and one packed-weight load covering the whole
-// stage; every lane copies scales with 4-byte cp.async -- K-slice h, rows
-// lane, lane + 32, ... to am_dst[h][row] -- and arrives on full[s] when its
-// copies land.  Rows past N and K-slices past the weight's last block copy a
-// harmless in-range scale (their products are never stored or multiply zeros).
+// Weight producer warp, one stage: lane 0 arms pfull[p] with the TMA byte
+// count and loads the packed tile of the whole stage (one box of 32 * KS
+// bytes x ROWS rows); every lane copies scales with 4-byte cp.async --
+// K-slice h, rows lane, lane + 32, ... to am_dst[h][row] -- and arrives on
+// pfull[p] when its copies land.  Rows past N and K-slices past the weight's
+// last block copy a harmless in-range scale (their products are never
+// stored or multiply zeros).
 template <int ROWS, int KS>
-__device__ __forceinline__ void produce_stage(const Barriers& bar, int s, int lane, uint32_t tx_bytes,
-                                              const CUtensorMap* tm_x, uint32_t x_dst, uint32_t x_bytes,
-                                              int x_col0, int x_row, const CUtensorMap* tm_w, uint32_t p_dst,
-                                              int p_col0, int n0, uint32_t am_dst, const float* absmax, int N,
-                                              int am_pitch, int kb_abs0) {
+__device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_t tx_bytes, const CUtensorMap* tm_w,
+                                                uint32_t p_dst, int p_col0, int n0, uint32_t am_dst,
+                                                const float* absmax, int N, int am_pitch, int kb_abs0) {
     if (lane == 0) {
-        mbar_arrive_expect_tx(bar.full(s), tx_bytes);
-#pragma unroll
-        for (int h = 0; h < KS; ++h)
-            tma_load_2d(x_dst + h * x_bytes, tm_x, bar.full(s), x_col0 + h * kBK, x_row);
-        tma_load_2d(p_dst, tm_w, bar.full(s), p_col0, n0);
+        mbar_arrive_expect_tx(full, tx_bytes);
+        tma_load_2d(p_dst, tm_w, full, p_col0, n0);
     }
 #pragma unroll
     for (int h = 0; h < KS; ++h) {
@@ -201,7 +214,7 @@ __device__ __forceinline__ void produce_stage(const Barriers& bar, int s, int la
             cp_async_4(am_dst + 4u * (h * ROWS + i), src);
         }
     }
-    cp_async_arrive_noinc(bar.full(s));
+    cp_async_arrive_noinc(full);
 }
 
 // ============================================================ the kernel
@@ -215,37 +228,58 @@ struct TsCfg {
     static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
     static constexpr int P_BYTES = BW * kPackedRow * KS;
     static constexpr int AM_BYTES = BW * 4 * KS;
-    static constexpr int SLOT_BYTES = KS * XB + P_BYTES + AM_BYTES;
+    static constexpr int X_SLOT = KS * XB;                               // activation ring slot
+    static constexpr int P_SLOT = (P_BYTES + AM_BYTES + 1023) / 1024 * 1024;   // weight ring slot
     static constexpr int TMEM_COLS = 512;
-    static constexpr int A_COL0 = NX <= 32 ? 32 : (NX + 31) / 32 * 32;   // accumulator in [0, NX)
+    // NACC independent accumulators of NX columns each (MMA j of a K-slice
+    // goes to accumulator j % NACC; the epilogue sums them): a narrow MMA
+    // finishes faster than the accumulate chain turns around, so a single
+    // accumulator would serialise small-NX tiles.
+    static constexpr int NACC = NX <= 32 ? 4 : (NX <= 64 ? 2 : 1);
+    static constexpr int ACC_STRIDE = (NX + 31) / 32 * 32;        // accumulator a at column a * ACC_STRIDE
+    static constexpr int A_COL0 = NACC * ACC_STRIDE;
+    // MMA issuers: a narrow MMA costs its issuing thread about as much as a
+    // wide one, so small-NX tiles issue from two threads.  Issuer i takes the
+    // K-slices h = i (mod MI) of every stage into its own NACC / MI
+    // accumulators, which keeps each accumulator's summation order fixed.
+    static constexpr int MI = (NACC >= 2 && KS >= 2) ? 2 : 1;
+    static constexpr int ACC_PER_MI = NACC / MI;
     static constexpr int A_SLOT = 32 * KS;              // 64 bf16 per row per K-slice = 32 columns
     static constexpr int TMEM_SLOTS = (TMEM_COLS - A_COL0) / A_SLOT;
     static constexpr int SMEM_LIMIT = 232448;
-    static constexpr int SMEM_SLOTS = (SMEM_LIMIT - 2048) / SLOT_BYTES;
-    static constexpr int S = TMEM_SLOTS < SMEM_SLOTS ? (TMEM_SLOTS < 8 ? TMEM_SLOTS : 8)
-                                                     : (SMEM_SLOTS < 8 ? SMEM_SLOTS : 8);
-    static constexpr int OFF_P = S * KS * XB;
-    static constexpr int OFF_AM = OFF_P + S * P_BYTES;
-    static constexpr int OFF_BAR = OFF_AM + S * AM_BYTES;
+    static constexpr int BUDGET = SMEM_LIMIT - 2048;    // alignment slack, barriers
+    static constexpr int cmin(int a, int b) { return a < b ? a : b; }
+    static constexpr int ST = cmin(TMEM_SLOTS, 8);
+    // activation slots, at most ST (so a wait on done[] never falls two
+    // phases behind), leaving room for 3 weight slots
+    static constexpr int SX = cmin(ST, (BUDGET - 3 * P_SLOT) / X_SLOT);
+    static constexpr int SP = cmin(8, (BUDGET - SX * X_SLOT) / P_SLOT);
+    static constexpr int OFF_P = SX * X_SLOT;           // weight slot p: packed, then scales
+    static constexpr int OFF_BAR = OFF_P + SP * P_SLOT;
     // At least 120 KB, so no two CTAs share an SM: a second CTA there would
     // wait in tcgen05.alloc for the first one's 512 TMEM columns while
     // another SM idles.
-    static constexpr size_t USED = 1024 + OFF_BAR + Barriers::count(S) * 8 + 16;
+    static constexpr size_t USED = 1024 + OFF_BAR + Barriers::count(SX, ST, SP) * 8 + 16;
     static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
-    static constexpr int CONV_WARPS = 4 * KS * RS;      // warp 2 + 4u + q: unit u, TMEM lane quarter q
-    static constexpr int THREADS = 64 + 32 * CONV_WARPS;
+    // warps: 0 activation producer, 1 MMA issuer, 2 .. 2 + CONV_WARPS - 1
+    // converters (warp 2 + 4u + q: unit u, TMEM lane quarter q), then the
+    // second MMA issuer (MI == 2) and the weight producer
+    static constexpr int CONV_WARPS = 4 * KS * RS;
+    static constexpr int ISSUER1_WARP = 2 + CONV_WARPS;
+    static constexpr int WPROD_WARP = 2 + CONV_WARPS + (MI - 1);
+    static constexpr int THREADS = 32 * (WPROD_WARP + 1);
     static_assert(NX % 16 == 0 && NX >= 16 && NX <= 256, "MMA N");
     static_assert(XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
-    static_assert(S >= 2, "at least two stages");
+    static_assert(SX >= 2 && ST >= SX && SP >= 3, "ring depths");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
     static_assert(32 * KS <= 256, "packed-weight box width");
     static_assert(RS == 1 || RS == 2, "converter threads per row");
     static_assert(KS == 1 || KS == 2 || KS == 4, "packed rows of 32, 64 or 128 bytes");
     // The packed tile is loaded with the TMA swizzle whose span equals its
-    // row (32 * KS bytes): 16-byte chunk c of row r lands at chunk
-    // c ^ ((r * 32 * KS / 128) mod 32 * KS / 16).  A converter warp reads
-    // one chunk from each of 32 consecutive rows; the swizzle spreads them
-    // over all 32 banks, where plain rows would put them on the same four.
+    // row (32 * KS bytes): the 16-byte chunk at byte offset o lands at chunk
+    // (o / 16) XOR ((o / 128) mod 2 KS).  A converter warp reads one chunk
+    // from each of 32 consecutive rows; the swizzle spreads them over all 32
+    // banks, where plain rows would put them on the same four.
     static constexpr uint32_t SWZ_MASK = 2 * KS - 1;
     __device__ static uint32_t packed_offset(int row, int chunk) {
         const uint32_t o = static_cast<uint32_t>(row * kPackedRow * KS + 16 * chunk);
@@ -269,17 +303,19 @@ __global__ void __launch_bounds__(TsCfg<NX, KS, RS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
     using C = TsCfg<NX, KS, RS>;
-    constexpr int S = C::S;
+    constexpr int SX = C::SX;
+    constexpr int ST = C::ST;
+    constexpr int SP = C::SP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + Barriers::count(S));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + Barriers::count(SX, ST, SP));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const Barriers bar{smem_u32(bar_mem), S};
+    const Barriers bar{smem_u32(bar_mem), SX, ST, SP};
 
     auto x_tile = [&](int s, int h) { return smem + (s * KS + h) * C::XB; };
-    auto p_tile = [&](int s) { return smem + C::OFF_P + s * C::P_BYTES; };
-    auto am_tile = [&](int s) { return reinterpret_cast<const float*>(smem + C::OFF_AM + s * C::AM_BYTES); };
+    auto p_tile = [&](int p) { return smem + C::OFF_P + p * C::P_SLOT; };
+    auto am_tile = [&](int p) { return reinterpret_cast<const float*>(smem + C::OFF_P + p * C::P_SLOT + C::P_BYTES); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -293,7 +329,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int nst = (nk + KS - 1) / KS;   // stages; the last may hold fewer than KS K-slices
 
     if (threadIdx.x == 0) {
-        init_barriers(bar, C::CONV_WARPS);
+        init_barriers(bar, C::CONV_WARPS, C::MI);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -311,50 +347,82 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer warp
+        // ---------------- activation producer: lane 0 refills activation slot
+        // s with the stage's KS tiles once the MMAs that read it (stage st - SX)
+        // completed
+        if (lane == 0) {
+            int issued = 0;
+            for (int st = 0; st < nst; ++st) {
+                const int s = st % SX;
+                const int prev = st - SX;
+                if (prev >= 0 &&
+                    !mbar_wait(bar.done(prev % ST), (prev / ST) & 1, args.err, abort_flag, kErrTimeoutEmpty))
+                    break;
+                if (*abort_flag) break;
+                const int kb = kb0 + st * KS;
+                mbar_arrive_expect_tx(bar.xfull(s), C::X_SLOT);
+#pragma unroll
+                for (int h = 0; h < KS; ++h)
+                    tma_load_2d(smem_u32(x_tile(s, h)), &tm_x, bar.xfull(s), (kb + h) * kBK, m0);
+                ++issued;
+            }
+            if (*abort_flag) drain_ring(bar.xfull(0), SX, issued, args.err);
+        }
+    } else if (warp == C::WPROD_WARP) {
+        // ---------------- weight producer: refills weight slot p as soon as
+        // every converter warp has read the stage that held it
         int issued = 0;
         for (int st = 0; st < nst; ++st) {
-            const int s = st % S;
+            const int p = st % SP;
             bool ok = true;
-            if (st >= S) ok = mbar_wait(bar.done(s), ((st / S) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (st >= SP) ok = mbar_wait(bar.pempty(p), ((st / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             const int kb = kb0 + st * KS;
-            produce_stage<C::BW, KS>(bar, s, lane, KS * C::XB + C::P_BYTES, &tm_x, smem_u32(x_tile(s, 0)), C::XB,
-                                     kb * kBK, m0, &tm_w, smem_u32(p_tile(s)), kb * kPackedRow, n0,
-                                     smem_u32(am_tile(s)), args.absmax, args.N, nk_total, kb);
+            produce_weights<C::BW, KS>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)), kb * kPackedRow,
+                                       n0, smem_u32(am_tile(p)), args.absmax, args.N, nk_total, kb);
             ++issued;
         }
-        if (*abort_flag && lane == 0) drain_tma(bar, issued, args.err);
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: one wait, one fence and one commit per
-        // stage.  The converters arrive on conv only after observing full[s],
-        // so conv also orders the TMA's activation tiles before the MMAs.
+        if (*abort_flag && lane == 0) drain_ring(bar.pfull(0), SP, issued, args.err);
+    } else if (warp == 1 || (C::MI == 2 && warp == C::ISSUER1_WARP)) {
+        // ---------------- MMA issuer(s): per stage, wait for the converted
+        // weights and the activation tiles, one fence, the MMAs, one commit
+        const int issuer = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, NX);
+            // the activation-tile descriptors differ only in the start-address
+            // field (low 14 bits): one base plus a compile-time or per-stage offset
+            const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_tile(0, 0)));
+            const uint32_t x_lo0 = static_cast<uint32_t>(xdesc0);
+            const uint32_t x_hi = static_cast<uint32_t>(xdesc0 >> 32);
+            const uint32_t acc0 = tmem + issuer * C::ACC_PER_MI * C::ACC_STRIDE;
             bool ok = true;
             for (int st = 0; st < nst && ok; ++st) {
-                const int s = st % S;
-                ok = mbar_wait(bar.conv(s), (st / S) & 1, args.err, abort_flag, kErrTimeoutConverted);
+                const int s = st % SX;
+                const int t = st % ST;
+                ok = mbar_wait(bar.conv(t), (st / ST) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
+                     mbar_wait(bar.xfull(s), (st / SX) & 1, args.err, abort_flag, kErrTimeoutFull);
                 if (!ok) break;
                 tc_fence_after();
                 const int kbs = min(KS, nk - st * KS);
-                const uint32_t a_col = tmem + C::A_COL0 + s * C::A_SLOT;
+                const uint32_t a_col = tmem + C::A_COL0 + t * C::A_SLOT;
+                const uint32_t x_lo = x_lo0 + static_cast<uint32_t>((s * KS * C::XB) >> 4);
+                const uint32_t first = st > 0 ? 1u : 0u;   // accumulate into what earlier stages left
 #pragma unroll
                 for (int h = 0; h < KS; ++h) {
-                    if (h < kbs) {
-                        const uint32_t x0 = smem_u32(x_tile(s, h));
+                    if (h % C::MI == issuer && h < kbs) {
 #pragma unroll
                         for (int j = 0; j < kBK / 16; ++j)
-                            mma_bf16_ts(tmem, a_col + 32 * h + 8 * j, smem_desc_sw128(x0 + 32 * j), idesc,
-                                        (st > 0 || h > 0 || j > 0) ? 1u : 0u);
+                            mma_bf16_ts2(acc0 + (j % C::ACC_PER_MI) * C::ACC_STRIDE, a_col + 32 * h + 8 * j,
+                                         x_lo + static_cast<uint32_t>((h * C::XB + 32 * j) >> 4), x_hi, idesc,
+                                         (h >= C::MI || j >= C::ACC_PER_MI) ? 1u : first);
                     }
                 }
-                mma_commit(bar.done(s));
+                mma_commit(bar.done(t));
             }
             if (ok)
                 mma_commit(bar.accum());
             else
-                drain_mma(bar, args.err);
+                drain_mma(bar, issuer, args.err);
         }
     } else {
         // ---------------- converters: unit u = (warp - 2) / 4 converts part
@@ -369,23 +437,37 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const CodebookRegs cb = codebook_regs();
         bool ok = true;
         for (int st = 0; st < nst; ++st) {
-            const int s = st % S;
-            // Observing full[s] also orders this stage after the MMAs that last
-            // read TMEM slot s: the producer refilled slot s only after done[s].
-            const bool got = mbar_wait(bar.full(s), (st / S) & 1, args.err, abort_flag, kErrTimeoutFull);
+            const int t = st % ST;
+            const int p = st % SP;
+            // the stage's packed tile and scales; from the second use of TMEM
+            // slot t on, also the completion of the MMAs that last read it
+            bool got = mbar_wait(bar.pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
+            if (got && st >= ST)
+                got = mbar_wait(bar.done(t), ((st / ST) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            if (st * KS + h < nk) {
-                const float am = am_tile(s)[h * C::BW + r];
-                const uint32_t am2 = pack_bf16x2(am, am);
-                const uint8_t* ptile = p_tile(s);
-                const uint32_t col = lane_addr + C::A_COL0 + s * C::A_SLOT + 32 * h;
+            const bool active = st * KS + h < nk;   // warp-uniform
+            const uint8_t* ptile = p_tile(p);
+            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+            float am = 0.0f;
+            if (active) {
+                am = am_tile(p)[h * C::BW + r];
                 if constexpr (RS == 1) {
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h));
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + 1));
+                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h));
+                    q1 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + 1));
+                } else {
+                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + part));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.pempty(p));   // this warp is done with weight slot p
+            if (active) {
+                const uint32_t am2 = pack_bf16x2(am, am);
+                const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
+                if constexpr (RS == 1) {
                     uint32_t v[32];
                     expand8(q0.x, cb, am2, v + 0);
                     expand8(q0.y, cb, am2, v + 4);
@@ -398,7 +480,6 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     tmem_st32(col, v);
                 } else {
                     // 16 packed bytes = 32 values = 16 TMEM columns
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + part));
                     uint32_t v[16];
                     expand8(q0.x, cb, am2, v + 0);
                     expand8(q0.y, cb, am2, v + 4);
@@ -410,7 +491,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(s));
+            if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(t));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
@@ -424,6 +505,17 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 uint32_t v[16];
                 tmem_ld16(lane_addr + c0, v);
                 tmem_ld_wait();
+                // accumulators of an issuer that had no K-slice were never written
+                const int nacc = min(C::MI, min(KS, nk)) * C::ACC_PER_MI;
+#pragma unroll
+                for (int a = 1; a < C::NACC; ++a) {
+                    if (a >= nacc) break;
+                    uint32_t w[16];
+                    tmem_ld16(lane_addr + a * C::ACC_STRIDE + c0, w);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+                }
                 if (n < args.N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
