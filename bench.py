@@ -12,7 +12,9 @@ bf16 ~ N(0, 1) = 2 prompts x 1024 tokens):
 
 `value` is the linear FLOPs of a step (2*M*N*K for both calls) divided by the
 step time, summed over ranks (replicas, weak scaling).  Inputs are resident in
-HBM; an L2 flush (a 512 MiB memset, outside the events) precedes every step.
+HBM; an L2 flush precedes every step, outside the events: a 512 MiB memset,
+then a read of another 256 MiB so the step starts on clean L2 lines instead
+of paying for the memset's write-backs.
 Per-kernel times come from CUDA events around each call on the launching
 stream.  `e2e` repeats the step through the public API with W and X copied
 from pinned host memory and Y, Ys copied back inside the timed region.
@@ -256,7 +258,8 @@ def run_reference(args):
 def config_block(args):
     return {"workload": CFG.name, "M": CFG.m, "N": CFG.n, "K": CFG.k, "skinny_M": SKINNY_M,
             "block": 64, "absmax": "fp32", "w_dist": "N(0,0.02) bf16", "x_dist": "N(0,1) bf16",
-            "seeds": {"w": CFG.w_seed, "x": CFG.x_seed}, "l2": "flushed before every step (512 MiB memset)",
+            "seeds": {"w": CFG.w_seed, "x": CFG.x_seed},
+            "l2": "flushed before every step: 512 MiB memset, then a 256 MiB read (clean lines)",
             "parallelism": f"replicas{args.gpus}"}
 
 
@@ -287,6 +290,11 @@ def run_ours(args):
     assert st == nf4.NF4_OK
     wsp = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_read = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_read.max()
 
     names = ["nf4_quantize", "nf4_dequantize", "nf4_linear_m2048", "nf4_linear_m16"]
     calls = [
@@ -305,7 +313,7 @@ def run_ours(args):
                 evs[i][1].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
@@ -313,7 +321,6 @@ def run_ours(args):
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
-    call_ev = [[(mk(), mk()) for _ in calls] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     launches0 = nf4.nf4_launch_count()
     barrier(ws)
@@ -321,9 +328,9 @@ def run_ours(args):
     sampler.start()
     t_wall = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step_ev[k][0].record(stream)
-        step(call_ev[k])
+        step()
         step_ev[k][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -332,12 +339,20 @@ def run_ours(args):
     launches = nf4.nf4_launch_count() - launches0
     if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
         raise RuntimeError("a kernel reported a timeout in the timed region")
-
     step_ms = sum(a.elapsed_time(b) for a, b in step_ev)
-    per_call = [statistics.mean(call_ev[k][i][0].elapsed_time(call_ev[k][i][1]) for k in range(args.steps))
-                for i in range(len(calls))]
     step_ms = allreduce_max(step_ms, ws, dev)
     value = aggregate_tflops(FLOPS_PER_STEP, args.steps, step_ms, ws)
+
+    # ---- per-call breakdown: a second pass with events around every call
+    # (kept out of the timed steps above, whose value they would inflate)
+    call_steps = min(args.steps, 50)
+    call_ev = [[(mk(), mk()) for _ in calls] for _ in range(call_steps)]
+    for k in range(call_steps):
+        flush_l2()
+        step(call_ev[k])
+    torch.cuda.synchronize()
+    per_call = [statistics.mean(call_ev[k][i][0].elapsed_time(call_ev[k][i][1]) for k in range(call_steps))
+                for i in range(len(calls))]
 
     # ---- end to end through the public API, host buffers
     w_h = w.cpu().pin_memory()
@@ -354,13 +369,13 @@ def run_ours(args):
         ys_h.copy_(ys, non_blocking=True)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         e2e_step()
     e2e_ev = [(mk(), mk()) for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         e2e_ev[k][0].record(stream)
         e2e_step()
         e2e_ev[k][1].record(stream)
@@ -381,13 +396,13 @@ def run_ours(args):
     sk_bytes = numel * 0.5625 + 2 * SKINNY_M * CFG.k + 2 * SKINNY_M * CFG.n
     sk_gbs = sk_bytes / (t_s * 1e-3) / 1e9
     clocks = sampler.summary()
-    traffic = profiled_traffic("gemm_kernel")
+    traffic = profiled_traffic("ts_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(args),
-        "roofline": {"bound": "tensor", "kernel": "gemm_kernel (nf4_linear, M=2048)",
+        "roofline": {"bound": "tensor", "kernel": "ts_kernel (nf4_linear, M=2048)",
                      "achieved": lin_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": lin_tflops / pk["bf16_tflops"], "peak_source": f"bf16_tflops of {pk_kind}",
                      "traffic": traffic, "algorithmic": "2*M*N*K FLOP per launch"},
@@ -455,33 +470,50 @@ def stack_block(dev, passes: int = 2):
         for c, x, p, a, _ in entries:
             nf4.dequantize(p, a, c.n * c.k, out=deq[: c.n * c.k])
 
-    res = {}
-    for name, fn in (("linear", linear_pass), ("dequantize", dequant_pass)):
-        fn()                                  # warm: descriptors, kernel attributes
+    def timed(run):
         times = []
         for _ in range(passes):
             e0, e1 = mk(), mk()
             torch.cuda.synchronize()
             e0.record(stream)
-            fn()
+            run()
             e1.record(stream)
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
-        res[name] = min(times)
+        return min(times)
+
+    res, res_graph = {}, {}
+    for name, fn in (("linear", linear_pass), ("dequantize", dequant_pass)):
+        fn()                                  # warm: descriptors, kernel attributes
+        res[name] = timed(fn)
+        # the same 336 launches captured once as a CUDA graph and replayed:
+        # no host launch gaps between the short kernels
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        graph.replay()
+        res_graph[name] = timed(graph.replay)
+        del graph
     if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
         raise RuntimeError("a kernel reported a timeout in the stack passes")
     pk, _ = peaks()
     deq_bytes = params * BYTES_PER_W_DEQUANT
+    lin_tf = lambda ms: flops / (ms * 1e-3) / 1e12  # noqa: E731
+    deq_gbs = lambda ms: deq_bytes / (ms * 1e-3) / 1e9  # noqa: E731
     out = {
         "workload": f"gemma3_12b_48_layers_x_7_projections_m{workloads.STACK_M}",
         "weights": len(entries), "params": params,
-        "linear": {"ms": res["linear"], "TFLOP/s": flops / (res["linear"] * 1e-3) / 1e12,
-                   "frac_bf16": flops / (res["linear"] * 1e-3) / 1e12 / pk["bf16_tflops"], "flop": flops},
-        "dequantize": {"ms": res["dequantize"], "GB/s": deq_bytes / (res["dequantize"] * 1e-3) / 1e9,
-                       "frac_hbm": deq_bytes / (res["dequantize"] * 1e-3) / 1e9 / pk["hbm_gbs"], "bytes": deq_bytes},
+        "linear": {"ms": res_graph["linear"], "TFLOP/s": lin_tf(res_graph["linear"]),
+                   "frac_bf16": lin_tf(res_graph["linear"]) / pk["bf16_tflops"], "flop": flops,
+                   "eager": {"ms": res["linear"], "TFLOP/s": lin_tf(res["linear"])}},
+        "dequantize": {"ms": res_graph["dequantize"], "GB/s": deq_gbs(res_graph["dequantize"]),
+                       "frac_hbm": deq_gbs(res_graph["dequantize"]) / pk["hbm_gbs"], "bytes": deq_bytes,
+                       "eager": {"ms": res["dequantize"], "GB/s": deq_gbs(res["dequantize"])}},
         "quantize_once": {"ms": q_ms, "GB/s": params * BYTES_PER_W_QUANT / (q_ms * 1e-3) / 1e9,
                           "pages_one_time_s": 52.0},
-        "timing": f"best of {passes} passes, CUDA events around the whole pass; working set > L2",
+        "timing": (f"best of {passes} passes, CUDA events around the whole pass; each pass is the 336 "
+                   "calls replayed as one captured CUDA graph ('eager': the same calls launched one by "
+                   "one from Python); working set > L2"),
     }
     del entries, y, deq
     torch.cuda.empty_cache()
