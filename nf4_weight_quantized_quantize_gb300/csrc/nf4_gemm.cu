@@ -60,7 +60,9 @@ constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per
 //   done[t]    the stage's MMAs completed (one commit per MMA issuer): TMEM
 //              slot t may be rewritten, and the activation slot of stage st
 //              (st % SX) may be refilled
-//   pfull[p]   the stage's packed tile landed (TMA) and its scales were copied
+//   pfull[p]   the stage's packed tile landed (TMA) and its scales were copied;
+//              the weight producer issues these loads only after done[] of the
+//              stage's TMEM slot, so pfull also means "TMEM slot free"
 //   pempty[p]  every converter warp has read weight slot p
 // plus accum (the accumulators are final) and one drain barrier per MMA
 // issuer (error path only).
@@ -369,13 +371,18 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (*abort_flag) drain_ring(bar.xfull(0), SX, issued, args.err);
         }
     } else if (warp == C::WPROD_WARP) {
-        // ---------------- weight producer: refills weight slot p as soon as
-        // every converter warp has read the stage that held it
+        // ---------------- weight producer: refills weight slot p once every
+        // converter warp has read the stage that held it and, from the second
+        // use of the stage's TMEM slot on, once the MMAs that last read that
+        // slot completed -- so pfull alone tells a converter it may go ahead
+        // (one barrier wait per stage for the converter warps)
         int issued = 0;
         for (int st = 0; st < nst; ++st) {
             const int p = st % SP;
             bool ok = true;
             if (st >= SP) ok = mbar_wait(bar.pempty(p), ((st / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (ok && st >= ST)
+                ok = mbar_wait(bar.done(st % ST), ((st / ST) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             const int kb = kb0 + st * KS;
             produce_weights<C::BW, KS>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)), kb * kPackedRow,
@@ -439,11 +446,9 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         for (int st = 0; st < nst; ++st) {
             const int t = st % ST;
             const int p = st % SP;
-            // the stage's packed tile and scales; from the second use of TMEM
-            // slot t on, also the completion of the MMAs that last read it
-            bool got = mbar_wait(bar.pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
-            if (got && st >= ST)
-                got = mbar_wait(bar.done(t), ((st / ST) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            // the stage's packed tile and scales; the weight producer loaded
+            // them only after the MMAs that last read TMEM slot t completed
+            const bool got = mbar_wait(bar.pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
