@@ -45,87 +45,109 @@ __device__ __forceinline__ uint32_t quantize8(uint4 v, uint32_t am_bits, const f
 }
 
 // Fast code selection.  n = w / absmax is approximated by q = w * rcp(absmax)
-// with a correctly rounded reciprocal: |q - n| <= 3 * 2^-24 * |n|.  A uniform
-// grid of 65 cells of width 1/32 over [-1, 1] holds at most one threshold per
-// cell, and every threshold sits at least 1e-3 from a cell edge (checked at
-// compile time below), so the cell of q and the count of thresholds below it
-// are those of n.  Only the cell's own threshold can separate q from n, and
-// only when |q - t| <= 2^-20 |t|; such elements (a handful per billion) take
-// the exact path: IEEE division and the threshold search.
-constexpr int kCells = 65;
-constexpr double kCellWidth = 1.0 / 32.0;
+// with a correctly rounded reciprocal: |q - n| <= 3 * 2^-24 * |n| <= 2^-22.
+//
+// A degree-5 polynomial h, fitted to h(T_j) ~ j at the 15 thresholds and
+// monotone on [-1, 1], gives est = round(h(q)) with est in {code - 1, code}
+// for every fp32 q in [-1 - 4 ulp, 1 + 4 ulp] (the true code of q is the
+// number of thresholds below q).  That was checked for all 2.1e9 such q; h
+// stays at least 0.032 away from the rounding boundaries that would break
+// it, far above fp32 evaluation error.  So one comparison with T[est] (T[15]
+// = +inf) decides the code of q: code = est + (q > T[est]).  The codes of q
+// and n can only differ if a threshold lies between them, and the only
+// threshold near q is T[est]; such words (|q - T[est]| <= 2^-21, a few per
+// hundred thousand) are redone on the exact path.  The rounding to an
+// integer rides on the last FMA: adding 1.5 * 2^23 leaves round(h) in the
+// low mantissa bits, so the constant term (7) is kept an integer.
+constexpr float kH5 = 1.6238466501235962f;
+constexpr float kH4 = 1.0259608030319214f;
+constexpr float kH3 = -5.9369730949401855f;
+constexpr float kH2 = -0.9115704298019409f;
+constexpr float kH1 = 11.66257095336914f;
+constexpr float kH0Magic = 12582919.0f;          // 7 + 1.5 * 2^23, exact in fp32
+constexpr int kMagicBits = 0x4B400000;           // bits of 1.5 * 2^23
+constexpr float kGuard = 0x1p-21f;
 
-constexpr bool grid_is_safe() {
-    int prev_cell = -1;
-    for (int j = 0; j < 15; ++j) {
-        double t = static_cast<double>(threshold(j));
-        double x = (t + 1.0) / kCellWidth;
-        int cell = static_cast<int>(x);
-        double frac = x - cell;
-        if (cell <= prev_cell) return false;                      // one threshold per cell
-        if (frac * kCellWidth < 1e-3 || (1.0 - frac) * kCellWidth < 1e-3) return false;
-        prev_cell = cell;
-    }
-    return true;
+// Two fp32 lanes in one 64-bit register pair, for the packed f32x2 ops
+// (each lane rounds exactly like the scalar op).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
-static_assert(grid_is_safe(), "quantizer grid: thresholds must be one per cell and away from cell edges");
-
-struct QuantCell {
-    float t;          // the threshold inside the cell, or +inf
-    float guard;      // |t| * 2^-20: closer than this, decide exactly
-    uint32_t base;    // number of thresholds below the cell
-    uint32_t pad;
-};
-
-__device__ __forceinline__ void build_cells(QuantCell* cells, int tid, int nthreads) {
-    for (int i = tid; i < kCells; i += nthreads) {
-        const float lo = static_cast<float>(i) * 0.03125f - 1.0f;     // exact
-        const float hi = lo + 0.03125f;
-        QuantCell c{__int_as_float(0x7f800000), 0.0f, 0u, 0u};
-        for (int j = 0; j < 15; ++j) {
-            const float t = c_thr[j];
-            if (t < lo) ++c.base;
-            else if (t < hi) c.t = t, c.guard = fabsf(t) * 0x1p-20f;
-        }
-        cells[i] = c;
-    }
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
-__device__ __forceinline__ uint32_t fast_code(float q, const QuantCell* cells, bool& exact_needed) {
-    int idx = __float2int_rz(fmaf(q, 32.0f, 32.0f));
-    idx = min(max(idx, 0), kCells - 1);
-    const QuantCell c = cells[idx];
-    exact_needed |= !(fabsf(q - c.t) > c.guard);
-    return c.base + (q > c.t ? 1u : 0u);
+// Code of one quotient q given h(q) + 1.5 * 2^23 in `hm`.
+__device__ __forceinline__ uint32_t code_from_estimate(float q, float hm, const float* s_thr, bool& exact_needed) {
+    const int est = __float_as_int(hm) - kMagicBits;   // 0 .. 15
+    const float t = s_thr[est];
+    exact_needed |= !(fabsf(q - t) > kGuard);
+    return static_cast<uint32_t>(est) + (q > t ? 1u : 0u);
+}
+
+// The two codes of one bf16x2 word (element 2i in the low half): the
+// quotients and the polynomial run as f32x2 pairs.
+__device__ __forceinline__ uint32_t code_pair(uint32_t word, uint64_t rcp2, const float* s_thr, bool& exact_needed) {
+    const uint64_t q2 = mul_f32x2(pack_f32x2(__uint_as_float(word << 16), __uint_as_float(word & 0xffff0000u)), rcp2);
+    uint64_t h2 = fma_f32x2(pack_f32x2(kH5, kH5), q2, pack_f32x2(kH4, kH4));
+    h2 = fma_f32x2(h2, q2, pack_f32x2(kH3, kH3));
+    h2 = fma_f32x2(h2, q2, pack_f32x2(kH2, kH2));
+    h2 = fma_f32x2(h2, q2, pack_f32x2(kH1, kH1));
+    h2 = fma_f32x2(h2, q2, pack_f32x2(kH0Magic, kH0Magic));
+    float q0, q1, h0, h1;
+    unpack_f32x2(q2, q0, q1);
+    unpack_f32x2(h2, h0, h1);
+    const uint32_t c0 = code_from_estimate(q0, h0, s_thr, exact_needed);
+    const uint32_t c1 = code_from_estimate(q1, h1, s_thr, exact_needed);
+    return (c0 << 4) | c1;   // element 2i in the high nibble
 }
 
 // quantize8 with the fast path: one reciprocal per block, the exact path only
-// for elements the grid cannot decide.
-__device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, const QuantCell* cells,
-                                                   const float* s_thr) {
+// for words the estimate cannot decide.
+__device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, const float* s_thr) {
     if (am_bits == 0u) return 0x77777777u;
     const float am = __uint_as_float(am_bits << 16);
     const float rcp = __frcp_rn(am);
-    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out = 0;
+    const uint64_t rcp2 = pack_f32x2(rcp, rcp);
     bool exact_needed = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t c0 = fast_code(__uint_as_float(wd[i] << 16) * rcp, cells, exact_needed);
-        const uint32_t c1 = fast_code(__uint_as_float(wd[i] & 0xffff0000u) * rcp, cells, exact_needed);
-        out |= ((c0 << 4) | c1) << (8 * i);
-    }
+    const uint32_t out = code_pair(v.x, rcp2, s_thr, exact_needed) | (code_pair(v.y, rcp2, s_thr, exact_needed) << 8) |
+                         (code_pair(v.z, rcp2, s_thr, exact_needed) << 16) |
+                         (code_pair(v.w, rcp2, s_thr, exact_needed) << 24);
     return exact_needed ? quantize8(v, am_bits, s_thr) : out;
 }
 
+// Per-halfword unsigned max of two bf16x2 words.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest 15-bit magnitude pattern among the 8 bf16 of a 16-byte word,
+// reduced pairwise on both halves at once.
 __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
-    uint32_t m = max(max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu), max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu));
-    m = max(m, max(max(v.z & 0x7fffu, (v.z >> 16) & 0x7fffu), max(v.w & 0x7fffu, (v.w >> 16) & 0x7fffu)));
-    return m;
+    const uint32_t m2 = max_u16x2(max_u16x2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                  max_u16x2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu));
+    return max(m2 & 0xffffu, m2 >> 16);
 }
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;
+#ifndef NF4_QUANT_UNROLL
+#define NF4_QUANT_UNROLL 4
+#endif
+constexpr int kQuantUnroll = NF4_QUANT_UNROLL;   // 16-byte words in flight per thread
 
 // Vectorized quantizer for whole blocks.  Thread t of a warp owns the 16-byte
 // word t of a 512-byte warp tile (4 blocks); 8 lanes share a block and reduce
@@ -135,9 +157,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __restrict__ packed,
                     float* __restrict__ absmax) {
     __shared__ float s_thr[16];
-    __shared__ QuantCell s_cells[kCells];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
-    build_cells(s_cells, threadIdx.x, kQuantThreads);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
@@ -158,7 +178,7 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
             if (t0 + u * nwarps < ntiles && word < nwords) {
-                packed[word] = quantize8_fast(v[u], m, s_cells, s_thr);
+                packed[word] = quantize8_fast(v[u], m, s_thr);
                 if ((lane & 7) == 0) absmax[word >> 3] = __uint_as_float(m << 16);
             }
         }
