@@ -160,6 +160,17 @@ __device__ __forceinline__ void expand8(uint32_t p, const CodebookRegs& cb, uint
     o[3] = bf16x2_mul(prmt(lo, hi, 0x6273u), am2);
 }
 
+// expand8 through the shared-memory byte table instead of register permutes:
+// per packed byte one table load (the bf16 codebook values of its two codes,
+// element 2i in the low half) and one bf16x2 multiply.  `lut_lane` points at
+// this lane's column of the replicated table (entry b at lut_lane[32 b]).
+__device__ __forceinline__ void expand8_lut(uint32_t p, const uint32_t* lut_lane, uint32_t am2, uint32_t* o) {
+    o[0] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4440u)], am2);
+    o[1] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4441u)], am2);
+    o[2] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4442u)], am2);
+    o[3] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4443u)], am2);
+}
+
 // Whether a converter warp reports stage st as converted.  Always true in
 // the library.  A test build (-DNF4_TEST_DROP_CONVERTED_ARRIVE) withholds the
 // report for stage 0 -- a flag that nothing sets -- so the MMA issuer's bounded
@@ -224,7 +235,7 @@ __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_
 // Compile-time layout of one kernel instance: NX activation rows per tile
 // (MMA N), stages of KS K-slices, RS converter threads per weight row and
 // K-slice (each expands 64 / RS of the row's values).
-template <int NX, int KS, int RS>
+template <int NX, int KS, int RS, bool LUT>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
     static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
@@ -249,7 +260,10 @@ struct TsCfg {
     static constexpr int A_SLOT = 32 * KS;              // 64 bf16 per row per K-slice = 32 columns
     static constexpr int TMEM_SLOTS = (TMEM_COLS - A_COL0) / A_SLOT;
     static constexpr int SMEM_LIMIT = 232448;
-    static constexpr int BUDGET = SMEM_LIMIT - 2048;    // alignment slack, barriers
+    // LUT: a 256-entry bf16x2 byte table replicated once per lane (entry b of
+    // lane l at word 32 b + l, so a warp's lookups never share a bank)
+    static constexpr int LUT_BYTES = LUT ? 256 * 32 * 4 : 0;
+    static constexpr int BUDGET = SMEM_LIMIT - 2048 - LUT_BYTES;   // alignment slack, barriers
     static constexpr int cmin(int a, int b) { return a < b ? a : b; }
     static constexpr int ST = cmin(TMEM_SLOTS, 8);
     // activation slots, at most ST (so a wait on done[] never falls two
@@ -257,7 +271,8 @@ struct TsCfg {
     static constexpr int SX = cmin(ST, (BUDGET - 3 * P_SLOT) / X_SLOT);
     static constexpr int SP = cmin(8, (BUDGET - SX * X_SLOT) / P_SLOT);
     static constexpr int OFF_P = SX * X_SLOT;           // weight slot p: packed, then scales
-    static constexpr int OFF_BAR = OFF_P + SP * P_SLOT;
+    static constexpr int OFF_LUT = OFF_P + SP * P_SLOT;
+    static constexpr int OFF_BAR = OFF_LUT + LUT_BYTES;
     // At least 120 KB, so no two CTAs share an SM: a second CTA there would
     // wait in tcgen05.alloc for the first one's 512 TMEM columns while
     // another SM idles.
@@ -300,11 +315,11 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int KS, int RS, bool SPLIT>
-__global__ void __launch_bounds__(TsCfg<NX, KS, RS>::THREADS, 1)
+template <int NX, int KS, int RS, bool LUT, bool SPLIT>
+__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using C = TsCfg<NX, KS, RS>;
+    using C = TsCfg<NX, KS, RS, LUT>;
     constexpr int SX = C::SX;
     constexpr int ST = C::ST;
     constexpr int SP = C::SP;
@@ -330,6 +345,10 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int nk = min(args.kb_per_split, nk_total - kb0);
     const int nst = (nk + KS - 1) / KS;   // stages; the last may hold fewer than KS K-slices
 
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
+    if constexpr (LUT) {
+        for (int e = threadIdx.x; e < 256 * 32; e += C::THREADS) lut[e] = lut_entry(static_cast<uint32_t>(e >> 5));
+    }
     if (threadIdx.x == 0) {
         init_barriers(bar, C::CONV_WARPS, C::MI);
         *abort_flag = 0;
@@ -472,24 +491,31 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (active) {
                 const uint32_t am2 = pack_bf16x2(am, am);
                 const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
+                const uint32_t* lut_lane = lut + lane;
+                auto expand = [&](uint32_t word, uint32_t* o) {
+                    if constexpr (LUT)
+                        expand8_lut(word, lut_lane, am2, o);
+                    else
+                        expand8(word, cb, am2, o);
+                };
                 if constexpr (RS == 1) {
                     uint32_t v[32];
-                    expand8(q0.x, cb, am2, v + 0);
-                    expand8(q0.y, cb, am2, v + 4);
-                    expand8(q0.z, cb, am2, v + 8);
-                    expand8(q0.w, cb, am2, v + 12);
-                    expand8(q1.x, cb, am2, v + 16);
-                    expand8(q1.y, cb, am2, v + 20);
-                    expand8(q1.z, cb, am2, v + 24);
-                    expand8(q1.w, cb, am2, v + 28);
+                    expand(q0.x, v + 0);
+                    expand(q0.y, v + 4);
+                    expand(q0.z, v + 8);
+                    expand(q0.w, v + 12);
+                    expand(q1.x, v + 16);
+                    expand(q1.y, v + 20);
+                    expand(q1.z, v + 24);
+                    expand(q1.w, v + 28);
                     tmem_st32(col, v);
                 } else {
                     // 16 packed bytes = 32 values = 16 TMEM columns
                     uint32_t v[16];
-                    expand8(q0.x, cb, am2, v + 0);
-                    expand8(q0.y, cb, am2, v + 4);
-                    expand8(q0.z, cb, am2, v + 8);
-                    expand8(q0.w, cb, am2, v + 12);
+                    expand(q0.x, v + 0);
+                    expand(q0.y, v + 4);
+                    expand(q0.z, v + 8);
+                    expand(q0.w, v + 12);
                     tmem_st16(col + 16 * part, v);
                 }
                 tmem_st_wait();
@@ -577,6 +603,14 @@ constexpr int kKsDirect = NF4_KS_DIRECT;     // K-slices per stage, M >= 128
 constexpr int kKsSplit = NF4_KS_SPLIT;       // K-slices per stage, M < 128
 constexpr int kRsDirect = NF4_RS_DIRECT;     // converter threads per weight row, M >= 128
 constexpr int kRsSplit = 1;                  // converter threads per weight row, M < 128
+#ifndef NF4_LUT_DIRECT
+#define NF4_LUT_DIRECT 0
+#endif
+#ifndef NF4_LUT_SPLIT
+#define NF4_LUT_SPLIT 1
+#endif
+constexpr bool kLutDirect = NF4_LUT_DIRECT != 0;   // shared-memory byte table instead of register permutes
+constexpr bool kLutSplit = NF4_LUT_SPLIT != 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -661,12 +695,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, bool SPLIT>
+template <int NX, int KS, int RS, bool LUT, bool SPLIT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    using C = TsCfg<NX, KS, RS>;
+    using C = TsCfg<NX, KS, RS, LUT>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, RS, SPLIT>;
+    auto kernel = ts_kernel<NX, KS, RS, LUT, SPLIT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -677,32 +711,32 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS>
+template <bool SPLIT, int KS, int RS, bool LUT>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, RS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -722,8 +756,8 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
              p.m_tiles, dev.err_word};
-    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit>(dev, p, tm_x, tm_w, a, s)
-                   : dispatch_nx<false, kKsDirect, kRsDirect>(dev, p, tm_x, tm_w, a, s);
+    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit>(dev, p, tm_x, tm_w, a, s)
+                   : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect>(dev, p, tm_x, tm_w, a, s);
 }
 
 }  // namespace
