@@ -235,12 +235,15 @@ __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_
 // Compile-time layout of one kernel instance: NX activation rows per tile
 // (MMA N), stages of KS K-slices, RS converter threads per weight row and
 // K-slice (each expands 64 / RS of the row's values).
-template <int NX, int KS, int RS, bool LUT>
+template <int NX, int KS, int RS, bool LUT, int WS>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
     static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
-    static constexpr int P_BYTES = BW * kPackedRow * KS;
-    static constexpr int AM_BYTES = BW * 4 * KS;
+    // A weight-ring slot holds WS stages (WS * KS K-slices): the converter
+    // warps wait on it once per WS stages.
+    static constexpr int WK = KS * WS;                  // K-slices per weight slot
+    static constexpr int P_BYTES = BW * kPackedRow * WK;
+    static constexpr int AM_BYTES = BW * 4 * WK;
     static constexpr int X_SLOT = KS * XB;                               // activation ring slot
     static constexpr int P_SLOT = (P_BYTES + AM_BYTES + 1023) / 1024 * 1024;   // weight ring slot
     static constexpr int TMEM_COLS = 512;
@@ -289,17 +292,16 @@ struct TsCfg {
     static_assert(XB % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
     static_assert(SX >= 2 && ST >= SX && SP >= 3, "ring depths");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
-    static_assert(32 * KS <= 256, "packed-weight box width");
+    static_assert(WK == 1 || WK == 2 || WK == 4, "packed rows of 32, 64 or 128 bytes");
     static_assert(RS == 1 || RS == 2, "converter threads per row");
-    static_assert(KS == 1 || KS == 2 || KS == 4, "packed rows of 32, 64 or 128 bytes");
     // The packed tile is loaded with the TMA swizzle whose span equals its
-    // row (32 * KS bytes): the 16-byte chunk at byte offset o lands at chunk
-    // (o / 16) XOR ((o / 128) mod 2 KS).  A converter warp reads one chunk
+    // row (32 * WK bytes): the 16-byte chunk at byte offset o lands at chunk
+    // (o / 16) XOR ((o / 128) mod 2 WK).  A converter warp reads one chunk
     // from each of 32 consecutive rows; the swizzle spreads them over all 32
     // banks, where plain rows would put them on the same four.
-    static constexpr uint32_t SWZ_MASK = 2 * KS - 1;
+    static constexpr uint32_t SWZ_MASK = 2 * WK - 1;
     __device__ static uint32_t packed_offset(int row, int chunk) {
-        const uint32_t o = static_cast<uint32_t>(row * kPackedRow * KS + 16 * chunk);
+        const uint32_t o = static_cast<uint32_t>(row * kPackedRow * WK + 16 * chunk);
         return o ^ (((o >> 7) & SWZ_MASK) << 4);
     }
     static_assert(THREADS <= 1024, "block size");
@@ -315,11 +317,11 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int KS, int RS, bool LUT, bool SPLIT>
-__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT>::THREADS, 1)
+template <int NX, int KS, int RS, bool LUT, int WS, bool SPLIT>
+__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using C = TsCfg<NX, KS, RS, LUT>;
+    using C = TsCfg<NX, KS, RS, LUT, WS>;
     constexpr int SX = C::SX;
     constexpr int ST = C::ST;
     constexpr int SP = C::SP;
@@ -344,6 +346,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int kb0 = split * args.kb_per_split;
     const int nk = min(args.kb_per_split, nk_total - kb0);
     const int nst = (nk + KS - 1) / KS;   // stages; the last may hold fewer than KS K-slices
+    const int nws = (nst + WS - 1) / WS;  // weight-ring stages
 
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
     if constexpr (LUT) {
@@ -390,22 +393,25 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (*abort_flag) drain_ring(bar.xfull(0), SX, issued, args.err);
         }
     } else if (warp == C::WPROD_WARP) {
-        // ---------------- weight producer: refills weight slot p once every
-        // converter warp has read the stage that held it and, from the second
-        // use of the stage's TMEM slot on, once the MMAs that last read that
-        // slot completed -- so pfull alone tells a converter it may go ahead
-        // (one barrier wait per stage for the converter warps)
+        // ---------------- weight producer: refills weight slot p (WS stages)
+        // once every converter warp has read what it held and the MMAs that
+        // last read the TMEM slots of its stages completed -- so pfull alone
+        // tells a converter warp it may go ahead (one barrier wait per WS
+        // stages).  MMAs complete in order: waiting for the last of those
+        // stages' predecessors covers the others.
         int issued = 0;
-        for (int st = 0; st < nst; ++st) {
-            const int p = st % SP;
+        for (int ws = 0; ws < nws; ++ws) {
+            const int p = ws % SP;
             bool ok = true;
-            if (st >= SP) ok = mbar_wait(bar.pempty(p), ((st / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
-            if (ok && st >= ST)
-                ok = mbar_wait(bar.done(st % ST), ((st / ST) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            if (ws >= SP) ok = mbar_wait(bar.pempty(p), ((ws / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            const int prev = min(WS * ws + WS - 1, nst - 1) - ST;   // MMAs of stage `prev` must be done
+            if (ok && prev >= 0)
+                ok = mbar_wait(bar.done(prev % ST), (prev / ST) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
-            const int kb = kb0 + st * KS;
-            produce_weights<C::BW, KS>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)), kb * kPackedRow,
-                                       n0, smem_u32(am_tile(p)), args.absmax, args.N, nk_total, kb);
+            const int kb = kb0 + ws * C::WK;
+            produce_weights<C::BW, C::WK>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
+                                          kb * kPackedRow, n0, smem_u32(am_tile(p)), args.absmax, args.N, nk_total,
+                                          kb);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(bar.pfull(0), SP, issued, args.err);
@@ -462,67 +468,80 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const CodebookRegs cb = codebook_regs();
         bool ok = true;
-        for (int st = 0; st < nst; ++st) {
-            const int t = st % ST;
-            const int p = st % SP;
-            // the stage's packed tile and scales; the weight producer loaded
-            // them only after the MMAs that last read TMEM slot t completed
-            const bool got = mbar_wait(bar.pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
+        for (int ws = 0; ws < nws; ++ws) {
+            const int p = ws % SP;
+            // the packed tiles and scales of WS stages; the weight producer
+            // loaded them only after the MMAs that last read their TMEM slots
+            const bool got = mbar_wait(bar.pfull(p), (ws / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const bool active = st * KS + h < nk;   // warp-uniform
+            // read this thread's share of every stage of the slot, then free it
             const uint8_t* ptile = p_tile(p);
-            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-            float am = 0.0f;
-            if (active) {
-                am = am_tile(p)[h * C::BW + r];
-                if constexpr (RS == 1) {
-                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h));
-                    q1 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + 1));
-                } else {
-                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + part));
+            uint4 q0[WS], q1[WS];
+            float am[WS];
+#pragma unroll
+            for (int w = 0; w < WS; ++w) {
+                const int st = WS * ws + w;
+                const int ks = w * KS + h;                   // K-slice within the weight slot
+                q0[w] = make_uint4(0, 0, 0, 0);
+                q1[w] = make_uint4(0, 0, 0, 0);
+                am[w] = 0.0f;
+                if (st < nst && st * KS + h < nk) {          // warp-uniform
+                    am[w] = am_tile(p)[ks * C::BW + r];
+                    if constexpr (RS == 1) {
+                        q0[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks));
+                        q1[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks + 1));
+                    } else {
+                        q0[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks + part));
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar.pempty(p));   // this warp is done with weight slot p
-            if (active) {
-                const uint32_t am2 = pack_bf16x2(am, am);
-                const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
-                const uint32_t* lut_lane = lut + lane;
-                auto expand = [&](uint32_t word, uint32_t* o) {
-                    if constexpr (LUT)
-                        expand8_lut(word, lut_lane, am2, o);
-                    else
-                        expand8(word, cb, am2, o);
-                };
-                if constexpr (RS == 1) {
-                    uint32_t v[32];
-                    expand(q0.x, v + 0);
-                    expand(q0.y, v + 4);
-                    expand(q0.z, v + 8);
-                    expand(q0.w, v + 12);
-                    expand(q1.x, v + 16);
-                    expand(q1.y, v + 20);
-                    expand(q1.z, v + 24);
-                    expand(q1.w, v + 28);
-                    tmem_st32(col, v);
-                } else {
-                    // 16 packed bytes = 32 values = 16 TMEM columns
-                    uint32_t v[16];
-                    expand(q0.x, v + 0);
-                    expand(q0.y, v + 4);
-                    expand(q0.z, v + 8);
-                    expand(q0.w, v + 12);
-                    tmem_st16(col + 16 * part, v);
+#pragma unroll
+            for (int w = 0; w < WS; ++w) {
+                const int st = WS * ws + w;
+                if (st >= nst) break;
+                const int t = st % ST;
+                if (st * KS + h < nk) {                      // warp-uniform
+                    const uint32_t am2 = pack_bf16x2(am[w], am[w]);
+                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
+                    const uint32_t* lut_lane = lut + lane;
+                    auto expand = [&](uint32_t word, uint32_t* o) {
+                        if constexpr (LUT)
+                            expand8_lut(word, lut_lane, am2, o);
+                        else
+                            expand8(word, cb, am2, o);
+                    };
+                    if constexpr (RS == 1) {
+                        uint32_t v[32];
+                        expand(q0[w].x, v + 0);
+                        expand(q0[w].y, v + 4);
+                        expand(q0[w].z, v + 8);
+                        expand(q0[w].w, v + 12);
+                        expand(q1[w].x, v + 16);
+                        expand(q1[w].y, v + 20);
+                        expand(q1[w].z, v + 24);
+                        expand(q1[w].w, v + 28);
+                        tmem_st32(col, v);
+                    } else {
+                        // 16 packed bytes = 32 values = 16 TMEM columns
+                        uint32_t v[16];
+                        expand(q0[w].x, v + 0);
+                        expand(q0[w].y, v + 4);
+                        expand(q0[w].z, v + 8);
+                        expand(q0[w].w, v + 12);
+                        tmem_st16(col + 16 * part, v);
+                    }
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(t));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(t));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
@@ -611,6 +630,11 @@ constexpr int kRsSplit = 1;                  // converter threads per weight row
 #endif
 constexpr bool kLutDirect = NF4_LUT_DIRECT != 0;   // shared-memory byte table instead of register permutes
 constexpr bool kLutSplit = NF4_LUT_SPLIT != 0;
+#ifndef NF4_WS_DIRECT
+#define NF4_WS_DIRECT 1
+#endif
+constexpr int kWsDirect = NF4_WS_DIRECT;     // stages per weight-ring slot, M >= 128
+constexpr int kWsSplit = 1;                  // stages per weight-ring slot, M < 128
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -695,12 +719,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, bool LUT, bool SPLIT>
+template <int NX, int KS, int RS, bool LUT, int WS, bool SPLIT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    using C = TsCfg<NX, KS, RS, LUT>;
+    using C = TsCfg<NX, KS, RS, LUT, WS>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, RS, LUT, SPLIT>;
+    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -711,32 +735,32 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS, bool LUT>
+template <bool SPLIT, int KS, int RS, bool LUT, int WS>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, RS, LUT, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -746,7 +770,7 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
                         const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, float* ws,
                         cudaStream_t s) {
     CUtensorMap tm_x, tm_w;
-    const int ks = p.split ? kKsSplit : kKsDirect;
+    const int ks = p.split ? kKsSplit * kWsSplit : kKsDirect * kWsDirect;   // K-slices per weight slot
     // the packed box row is 32 * ks bytes; its swizzle span matches (TsCfg::packed_offset)
     const CUtensorMapSwizzle wsw = ks == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
                                  : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -756,8 +780,8 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
              p.m_tiles, dev.err_word};
-    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit>(dev, p, tm_x, tm_w, a, s)
-                   : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect>(dev, p, tm_x, tm_w, a, s);
+    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit>(dev, p, tm_x, tm_w, a, s)
+                   : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect>(dev, p, tm_x, tm_w, a, s);
 }
 
 }  // namespace
