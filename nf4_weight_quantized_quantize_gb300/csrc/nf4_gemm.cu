@@ -235,7 +235,7 @@ __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_
 // Compile-time layout of one kernel instance: NX activation rows per tile
 // (MMA N), stages of KS K-slices, RS converter threads per weight row and
 // K-slice (each expands 64 / RS of the row's values).
-template <int NX, int KS, int RS, bool LUT, int WS>
+template <int NX, int KS, int RS, int LUT, int WS>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
     static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
@@ -265,7 +265,10 @@ struct TsCfg {
     static constexpr int SMEM_LIMIT = 232448;
     // LUT: a 256-entry bf16x2 byte table replicated once per lane (entry b of
     // lane l at word 32 b + l, so a warp's lookups never share a bank)
-    static constexpr int LUT_BYTES = LUT ? 256 * 32 * 4 : 0;
+    // (LUT == 1: every converter warp uses it; LUT == 2: the warps of row
+    // part 1 use it and those of part 0 the register permutes, splitting the
+    // expansion between the shared-memory and ALU pipes)
+    static constexpr int LUT_BYTES = LUT != 0 ? 256 * 32 * 4 : 0;
     static constexpr int BUDGET = SMEM_LIMIT - 2048 - LUT_BYTES;   // alignment slack, barriers
     static constexpr int cmin(int a, int b) { return a < b ? a : b; }
     static constexpr int ST = cmin(TMEM_SLOTS, 8);
@@ -317,7 +320,7 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int KS, int RS, bool LUT, int WS, bool SPLIT>
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT>
 __global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
@@ -349,7 +352,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int nws = (nst + WS - 1) / WS;  // weight-ring stages
 
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
-    if constexpr (LUT) {
+    if constexpr (LUT != 0) {
         for (int e = threadIdx.x; e < 256 * 32; e += C::THREADS) lut[e] = lut_entry(static_cast<uint32_t>(e >> 5));
     }
     if (threadIdx.x == 0) {
@@ -511,7 +514,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
                     const uint32_t* lut_lane = lut + lane;
                     auto expand = [&](uint32_t word, uint32_t* o) {
-                        if constexpr (LUT)
+                        if (LUT == 1 || (LUT == 2 && part == 1))   // warp-uniform
                             expand8_lut(word, lut_lane, am2, o);
                         else
                             expand8(word, cb, am2, o);
@@ -628,8 +631,8 @@ constexpr int kRsSplit = 1;                  // converter threads per weight row
 #ifndef NF4_LUT_SPLIT
 #define NF4_LUT_SPLIT 1
 #endif
-constexpr bool kLutDirect = NF4_LUT_DIRECT != 0;   // shared-memory byte table instead of register permutes
-constexpr bool kLutSplit = NF4_LUT_SPLIT != 0;
+constexpr int kLutDirect = NF4_LUT_DIRECT;   // 1: shared-memory byte table instead of register permutes, 2: half each
+constexpr int kLutSplit = NF4_LUT_SPLIT;
 #ifndef NF4_WS_DIRECT
 #define NF4_WS_DIRECT 1
 #endif
@@ -719,7 +722,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, bool LUT, int WS, bool SPLIT>
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
     using C = TsCfg<NX, KS, RS, LUT, WS>;
@@ -735,7 +738,7 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS, bool LUT, int WS>
+template <bool SPLIT, int KS, int RS, int LUT, int WS>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
