@@ -146,6 +146,21 @@ __device__ __forceinline__ uint32_t scale_entry(uint32_t e, float am) {
     return pack_bf16x2(lo * am, hi * am);
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Wait until the kernel this one was launched after (programmatic dependent
+// launch, see launch_pdl) has completed and its memory is visible; a no-op
+// for a normal launch.  Every kernel calls it before its first global access.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel on the stream start its prologue (it still waits for
+// this one in pdl_wait before touching global memory).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -372,6 +372,8 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();                      // the previous kernel on the stream has finished
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ---------------- activation producer: lane 0 refills activation slot
@@ -598,6 +600,8 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 // Sum the split-K partials in split order and round once to bf16.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn,
                                      uint16_t* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < mn;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float acc = ws[i];
@@ -733,7 +737,8 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > 0x7fffffff || p.splits > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(p.splits));
-    kernel<<<grid, C::THREADS, C::SMEM, s>>>(tm_x, tm_w, a);
+    if (cudaError_t e = launch_pdl(kernel, grid, dim3(C::THREADS), C::SMEM, s, tm_x, tm_w, a); e != cudaSuccess)
+        return e;
     count_launches(1);
     return cudaGetLastError();
 }
@@ -812,7 +817,10 @@ cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, i
     const int64_t mn = M * N;
     const int threads = 256;
     const int grid = static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
-    splitk_reduce_kernel<<<grid, threads, 0, s>>>(static_cast<const float*>(workspace), p.splits, mn, y);
+    if (cudaError_t e = launch_pdl(splitk_reduce_kernel, grid, threads, 0, s, static_cast<const float*>(workspace),
+                                   p.splits, mn, y);
+        e != cudaSuccess)
+        return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -4,10 +4,32 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
 namespace nf4 {
+
+// Launch `kernel` with programmatic dependent launch allowed: its CTAs may
+// start while the previous kernel on the stream is still finishing, run
+// their prologue (shared tables, barriers, TMEM allocation), and wait in
+// pdl_wait() for that kernel to complete before touching global memory.
+// Without a previous kernel the wait returns at once.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DeviceInfo {
     int ordinal = -1;

@@ -159,6 +159,8 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
     __shared__ float s_thr[16];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
     __syncthreads();
+    pdl_wait();                 // the previous kernel on the stream has finished
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kQuantThreads) >> 5;
@@ -194,6 +196,8 @@ __global__ void quantize_scalar_kernel(const uint16_t* __restrict__ w, int64_t n
     __shared__ float s_thr[16];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
     __syncthreads();
+    pdl_wait();                 // the previous kernel on the stream has finished
+    pdl_launch_dependents();
     for (int64_t b = b0 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < b1;
          b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t lo = b * kBlock;
@@ -232,6 +236,8 @@ dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict_
     __shared__ uint32_t lut[256];
     for (int e = threadIdx.x; e < 256; e += kDequantThreads) lut[e] = lut_entry(static_cast<uint32_t>(e));
     __syncthreads();
+    pdl_wait();                 // the previous kernel on the stream has finished
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kDequantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kDequantThreads) >> 5;
@@ -277,6 +283,8 @@ __global__ void dequant_scalar_kernel(const uint8_t* __restrict__ packed,
     __shared__ uint32_t lut[256];
     for (int e = threadIdx.x; e < 256; e += blockDim.x) lut[e] = lut_entry(static_cast<uint32_t>(e));
     __syncthreads();
+    pdl_wait();                 // the previous kernel on the stream has finished
+    pdl_launch_dependents();
     for (int64_t j = j0 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < j1;
          j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint32_t v = scale_entry(lut[packed[j]], absmax[(2 * j) / kBlock]);
@@ -299,6 +307,7 @@ static int grid_for(const DeviceInfo& dev, const void* kernel, int threads, int6
 
 cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t numel, uint8_t* packed,
                             float* absmax, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
     const int64_t nblocks = (numel + kBlock - 1) / kBlock;
     const int64_t full = numel / kBlock;
     const bool aligned = (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
@@ -310,8 +319,9 @@ cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t nu
         const int64_t ntiles = (nwords + 31) / 32;
         const int grid = grid_for(dev, reinterpret_cast<const void*>(quantize_vec_kernel),
                                   kQuantThreads, (ntiles + kQuantThreads / 32 - 1) / (kQuantThreads / 32));
-        quantize_vec_kernel<<<grid, kQuantThreads, 0, s>>>(reinterpret_cast<const uint4*>(w), nwords,
-                                                          reinterpret_cast<uint32_t*>(packed), absmax);
+        e = launch_pdl(quantize_vec_kernel, grid, kQuantThreads, 0, s, reinterpret_cast<const uint4*>(w), nwords,
+                       reinterpret_cast<uint32_t*>(packed), absmax);
+        if (e != cudaSuccess) return e;
         count_launches(1);
         scalar_from = full;
     }
@@ -319,7 +329,8 @@ cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t nu
         const int64_t n = nblocks - scalar_from;
         const int threads = 128;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
-        quantize_scalar_kernel<<<grid, threads, 0, s>>>(w, numel, scalar_from, nblocks, packed, absmax);
+        e = launch_pdl(quantize_scalar_kernel, grid, threads, 0, s, w, numel, scalar_from, nblocks, packed, absmax);
+        if (e != cudaSuccess) return e;
         count_launches(1);
     }
     return cudaGetLastError();
@@ -327,6 +338,7 @@ cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t nu
 
 cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, const float* absmax,
                               int64_t numel, uint16_t* out, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
     const int64_t nbytes = numel / 2;
     const bool aligned = (reinterpret_cast<uintptr_t>(packed) % 4 == 0) &&
                          (reinterpret_cast<uintptr_t>(absmax) % 4 == 0) &&
@@ -340,8 +352,9 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
             const int64_t warp_items = (ntiles + kDequantTiles - 1) / kDequantTiles;
             const int grid = grid_for(dev, reinterpret_cast<const void*>(dequant_vec_kernel), kDequantThreads,
                                       (warp_items + kDequantThreads / 32 - 1) / (kDequantThreads / 32), 2);
-            dequant_vec_kernel<<<grid, kDequantThreads, 0, s>>>(
-                reinterpret_cast<const uint32_t*>(packed), absmax, ntiles, reinterpret_cast<uint4*>(out));
+            e = launch_pdl(dequant_vec_kernel, grid, kDequantThreads, 0, s, reinterpret_cast<const uint32_t*>(packed),
+                           absmax, ntiles, reinterpret_cast<uint4*>(out));
+            if (e != cudaSuccess) return e;
             count_launches(1);
         }
         scalar_from = ntiles * 512;
@@ -350,7 +363,8 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
         const int64_t n = nbytes - scalar_from;
         const int threads = 256;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 8 * static_cast<int64_t>(dev.sm_count)));
-        dequant_scalar_kernel<<<grid, threads, 0, s>>>(packed, absmax, scalar_from, nbytes, out);
+        e = launch_pdl(dequant_scalar_kernel, grid, threads, 0, s, packed, absmax, scalar_from, nbytes, out);
+        if (e != cudaSuccess) return e;
         count_launches(1);
     }
     return cudaGetLastError();
