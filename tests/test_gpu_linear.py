@@ -205,3 +205,49 @@ def test_workspace_reuse_and_user_workspace():
 
 def test_no_error_recorded():
     assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
+
+
+def test_cuda_graph_replay_matches_eager():
+    """The calls are stream-ordered with no host synchronisation, so a whole
+    step (quantize, dequantize, linear at M = 256 and M = 16) captures into a
+    CUDA graph; replays give the eager results bit for bit (the kernels are
+    deterministic) and match the oracle."""
+    rs = np.random.default_rng(7)
+    n, k = 640, 1536
+    w = torch.from_numpy((rs.standard_normal((n, k)) * 0.02).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    x = torch.from_numpy(rs.standard_normal((256, k)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    xs = x[:16].contiguous()
+    p = torch.empty(n * k // 2, dtype=torch.uint8, device=DEV)
+    a = torch.empty(n * k // 64, dtype=torch.float32, device=DEV)
+    wd = torch.empty(n * k, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(256, n, dtype=torch.bfloat16, device=DEV)
+    ys = torch.empty(16, n, dtype=torch.bfloat16, device=DEV)
+    _, ws_bytes = nf4.nf4_linear_workspace_size(16, n, k)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+
+    def step():
+        nf4.quantize(w, out=(p, a))
+        nf4.dequantize(p, a, n * k, out=wd)
+        nf4.linear(x, p, a, n, out=y)
+        nf4.linear(xs, p, a, n, out=ys, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (p, a, wd, y, ys)]
+    for t in (p, a, wd, y, ys):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for t in (p, a, wd, y, ys):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, ref in zip((p, a, wd, y, ys), eager):
+            assert torch.equal(got, ref)
+    assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
+    q = Quantized(workloads.bits(w.cpu()))
+    assert np.array_equal(p.cpu().numpy(), q.p) and np.array_equal(a.cpu().numpy(), q.a)
+    yref = oracle.linear(workloads.bits(x.cpu()), q.p, q.a, n)
+    assert row_err(f32_of_bits(workloads.bits(y.cpu())).astype(np.float64), yref) < TOL
