@@ -135,6 +135,23 @@ def test_tile_path_ragged_shapes(M, N, K):
     check(rand_bits((M, K), 1.0, M + K), q)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (500, 1250, 4096),     # 20 tiles, ragged M and N, 32 stages
+    (1024, 2048, 3840),    # 64 tiles (k_proj-like)
+    (2048, 640, 15360),    # long K: 40 tiles of 120 stages
+])
+def test_tile_path_larger_shapes(M, N, K):
+    """Larger ragged shapes on the tile path, against the oracle (sampled rows
+    for the larger ones), and determinism: two calls give identical bits."""
+    q = Quantized(rand_bits((N, K), 0.02, M + 3 * N))
+    x_bits = rand_bits((M, K), 1.0, K + M)
+    rows = None if M * N * K <= 500 * 1250 * 4096 else np.sort(
+        np.random.default_rng(M).choice(M, 40, replace=False))
+    y1, _ = check(x_bits, q, rows=rows)
+    y2 = run_linear(x_bits, q)
+    assert np.array_equal(y1, y2)
+
+
 @pytest.mark.parametrize("M", [1, 2, 7, 15, 16, 17, 31, 33, 48, 64, 65, 100, 112, 127])
 def test_skinny_path_all_widths(M):
     N, K = 640, 1536
