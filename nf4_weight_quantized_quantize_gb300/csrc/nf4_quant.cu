@@ -145,7 +145,7 @@ __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
 
 constexpr int kQuantThreads = 256;
 #ifndef NF4_QUANT_UNROLL
-#define NF4_QUANT_UNROLL 4
+#define NF4_QUANT_UNROLL 1
 #endif
 constexpr int kQuantUnroll = NF4_QUANT_UNROLL;   // 16-byte words in flight per thread
 
@@ -165,13 +165,22 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kQuantThreads) >> 5;
     const int64_t ntiles = (nwords + 31) >> 5;
-    for (int64_t t0 = warp; t0 < ntiles; t0 += nwarps * kQuantUnroll) {
-        uint4 v[kQuantUnroll];
+    // kQuantUnroll tiles per warp and iteration; the next iteration's words are
+    // loaded before this one's are converted, so each warp keeps a DRAM round
+    // trip in flight while it computes
+    auto load = [&](int64_t t0, uint4 (&v)[kQuantUnroll]) {
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t word = ((t0 + u * nwarps) << 5) + lane;
             v[u] = (t0 + u * nwarps < ntiles && word < nwords) ? ldg_nc_v4(w + word) : make_uint4(0, 0, 0, 0);
         }
+    };
+    uint4 v[kQuantUnroll], nv[kQuantUnroll];
+    if (warp < ntiles) load(warp, nv);
+    for (int64_t t0 = warp; t0 < ntiles; t0 += nwarps * kQuantUnroll) {
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) v[u] = nv[u];
+        if (t0 + nwarps * kQuantUnroll < ntiles) load(t0 + nwarps * kQuantUnroll, nv);
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t word = ((t0 + u * nwarps) << 5) + lane;
