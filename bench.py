@@ -70,10 +70,14 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+GEMM_SOURCES = ("nf4_device.cuh", "nf4_gemm.cu", "nf4_launch.h")   # what ts_kernel is built from
+
+
 def kernel_source_hash() -> str:
+    """Hash of the sources of the kernel the roofline reports (ts_kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nf4_weight_quantized_quantize_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in GEMM_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
