@@ -2,7 +2,7 @@
 
 The oracle follows the diffuseR page "Gemma3 NF4 on GPU" (pull request #39,
 Summary): NF4-packed projection weights, dequantized and multiplied at the
-compute dtype, with forward parity judged by cosine > 0.99.  What the page
+compute dtype, with forward parity checked by cosine > 0.99.  What the page
 leaves open (codebook, block 64, fp32 absmax, nibble order, tie rule) is
 fixed by the readings listed in the oracle's C file.  Each test below pins one
 of those against a published table, a closed form, an invariant, a library
