@@ -61,8 +61,11 @@ def _load():
         lib.oracle_quantize.argtypes = [P, I64, I32, P, P]
         lib.oracle_dequantize.argtypes = [P, P, I64, I32, P]
         lib.oracle_linear.argtypes = [P, I64, I64, P, P, I64, I32, P]
+        lib.oracle_gelu_tanh.argtypes = [P, I64, P]
+        lib.oracle_linear_geglu.argtypes = [P, I64, I64, P, P, I64, I32, P]
         for f in (lib.oracle_nearest_code, lib.oracle_quantize,
-                  lib.oracle_dequantize, lib.oracle_linear, lib.oracle_set_num_threads):
+                  lib.oracle_dequantize, lib.oracle_linear, lib.oracle_set_num_threads,
+                  lib.oracle_gelu_tanh, lib.oracle_linear_geglu):
             f.restype = None
         _lib = lib
         return lib
@@ -137,4 +140,29 @@ def linear(x_bits: np.ndarray, packed: np.ndarray, absmax: np.ndarray, n_out: in
         raise ValueError("packed/absmax do not match [n_out, K]")
     y = np.empty((M, n_out), dtype=np.float64)
     _load().oracle_linear(_ptr(x), M, K, _ptr(p), _ptr(a), n_out, block, _ptr(y))
+    return y
+
+
+def gelu_tanh(x: np.ndarray) -> np.ndarray:
+    """GELU (tanh form) of each value, fp64."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_gelu_tanh(_ptr(x), x.size, _ptr(y))
+    return y
+
+
+def linear_geglu(x_bits: np.ndarray, packed: np.ndarray, absmax: np.ndarray, n_ff: int,
+                 block: int = BLOCK) -> np.ndarray:
+    """gelu_tanh(X . Wg^T) * (X . Wu^T) in fp64, [M, n_ff], where the NF4 weight
+    covers [2 n_ff, K]: the gate rows, then the up rows."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D")
+    M, K = x.shape
+    p = np.ascontiguousarray(packed, dtype=np.uint8).ravel()
+    a = np.ascontiguousarray(absmax, dtype=np.float32).ravel()
+    if p.size * 2 != 2 * n_ff * K or a.size != (2 * n_ff * K + block - 1) // block:
+        raise ValueError("packed/absmax do not match [2 n_ff, K]")
+    y = np.empty((M, n_ff), dtype=np.float64)
+    _load().oracle_linear_geglu(_ptr(x), M, K, _ptr(p), _ptr(a), n_ff, block, _ptr(y))
     return y

@@ -27,7 +27,9 @@
  *     low nibble;
  *   - dequant by nibble unpack (not a lookup table):
  *     y = bf16_rne( float(bf16_rne(C[code])) * absmax ), one fp32 multiply;
- *   - linear: Y[m][n] = sum_k X[m][k] * Wdeq[n][k], accumulated in fp64.
+ *   - linear: Y[m][n] = sum_k X[m][k] * Wdeq[n][k], accumulated in fp64;
+ *   - gate/up pair (the Gemma3 MLP): gelu_tanh(gate) * up of two linears
+ *     whose weights are stacked into one [2F, K] tensor, in fp64.
  *
  * Every loop below is the definition written out, one element at a time.
  * OpenMP splits only the outermost independent loop (blocks or rows); it
@@ -190,4 +192,35 @@ void oracle_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packe
         }
     }
     free(wq);
+}
+
+/* ---- gate/up projection pair with the GELU gate ------------------------- */
+
+/* GELU in its tanh form (Hendrycks and Gimpel, "Gaussian Error Linear Units
+ * (GELUs)", arXiv:1606.08415, section 2), the activation between the gate and
+ * up projections of the Gemma3 MLP:
+ *   gelu(x) = x/2 * (1 + tanh( sqrt(2/pi) * (x + 0.044715 x^3) )),
+ * evaluated in fp64. */
+static double gelu_tanh(double x) {
+    const double k = sqrt(2.0 / acos(-1.0));
+    return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+}
+
+void oracle_gelu_tanh(const double* x, int64_t count, double* y) {
+    for (int64_t i = 0; i < count; ++i) y[i] = gelu_tanh(x[i]);
+}
+
+/* GeGLU of the gate and up projections held as ONE weight: W [2F][K] is the
+ * gate weight (rows 0 .. F-1) followed by the up weight (rows F .. 2F-1),
+ * quantized as one tensor.  With G = X . Wdeq^T [M][2F] from oracle_linear,
+ *   out[m][n] = gelu(G[m][n]) * G[m][F + n],   n < F,
+ * all in fp64. */
+void oracle_linear_geglu(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const float* absmax, int64_t F, int32_t block, double* out) {
+    double* g = (double*)malloc((size_t)(M * 2 * F) * sizeof(double));
+    oracle_linear(x, M, K, packed, absmax, 2 * F, block, g);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < F; ++n)
+            out[m * F + n] = gelu_tanh(g[m * 2 * F + n]) * g[m * 2 * F + F + n];
+    free(g);
 }

@@ -381,3 +381,62 @@ def test_oracle_digest_is_stable():
         for key in ("input_w", "input_x", "packed", "absmax", "dequant"):
             assert g[key] == d[key], (name, key)
         assert np.allclose(g["linear_first_row"], d["linear_first_row"], rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- gate/up pair (GeGLU)
+
+
+def test_gelu_tanh_closed_forms():
+    """gelu(0) = 0; gelu(x) - gelu(-x) = x exactly in real arithmetic (the
+    tanh terms cancel); for large |x| the tanh saturates so gelu(x) = x and
+    gelu(-x) = 0; near zero gelu(x) = x/2 + sqrt(2/pi) x^2 / 2 + O(x^4)."""
+    x = np.array([0.0, 1e-6, 0.25, 0.5, 1.0, 2.0, 3.0, 8.0, 30.0])
+    g, gm = oracle.gelu_tanh(x), oracle.gelu_tanh(-x)
+    assert g[0] == 0.0
+    assert np.allclose(g - gm, x, rtol=4e-16, atol=0)
+    assert g[-2] == 8.0 and g[-1] == 30.0 and gm[-2] == 0.0 and gm[-1] == 0.0
+    small = 0.5e-6 + math.sqrt(2 / math.pi) * 0.5e-12
+    assert abs(g[1] - small) <= 1e-18
+
+
+def test_gelu_tanh_matches_torch():
+    """torch's own tanh-approximate GELU in fp64 (a library routine)."""
+    x = np.linspace(-10, 10, 20001)
+    want = torch.nn.functional.gelu(torch.tensor(x, dtype=torch.float64), approximate="tanh").numpy()
+    assert np.max(np.abs(oracle.gelu_tanh(x) - want)) <= 2e-15
+
+
+def test_gelu_tanh_is_the_tanh_form_not_erf():
+    """Against the exact GELU x * Phi(x): the tanh form stays within 5e-4 of
+    it (largest gap near x = -2.7) but is not it."""
+    x = np.linspace(-6, 6, 12001)
+    exact = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in x])
+    gap = np.max(np.abs(oracle.gelu_tanh(x) - exact))
+    assert 4e-4 < gap < 5e-4
+
+
+def test_linear_geglu_brute_force_small():
+    """Gate rows first, up rows second, activation on the gate: a plain Python
+    restatement with math.fsum and math.tanh on a tiny case."""
+    rs = np.random.default_rng(21)
+    M, F, K = 3, 3, 128
+    w = bf16_bits_of(rs.normal(0, 0.05, 2 * F * K))
+    x = bf16_bits_of(rs.normal(0, 1, M * K)).reshape(M, K)
+    p, a = oracle.quantize(w)
+    y = oracle.linear_geglu(x, p, a, F)
+    wd = [float(v) for v in f32_of_bits(oracle.dequantize(p, a, 2 * F * K))]
+    xf = [float(v) for v in f32_of_bits(x.ravel())]
+
+    def dot(m, row):
+        return math.fsum(xf[m * K + k] * wd[row * K + k] for k in range(K))
+
+    def gelu(v):
+        return 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+
+    for m in range(M):
+        for n in range(F):
+            want = gelu(dot(m, n)) * dot(m, F + n)
+            assert abs(y[m, n] - want) <= 1e-13 * max(1.0, abs(want))
+    # swapping the halves gives a different answer on this case
+    swapped = [[gelu(dot(m, F + n)) * dot(m, n) for n in range(F)] for m in range(M)]
+    assert np.max(np.abs(y - np.array(swapped))) > 1e-3
