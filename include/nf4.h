@@ -129,6 +129,35 @@ NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uin
                       const float* absmax, int64_t N, int32_t block, uint16_t* y,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * nf4_linear_geglu -- the gate and up projections of a Gemma3 MLP in one
+ * fused NF4 GEMM, with the GELU-gated product as its epilogue:
+ *   y[m][n] = bf16( gelu_tanh(G[m][n]) * G[m][F + n] ),   G = X . deq(W)^T,
+ * gelu_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))) (the tanh
+ * form of GELU, Hendrycks and Gimpel, arXiv:1606.08415, section 2).  The
+ * diffuseR page "Gemma3 NF4 on GPU" (#39), Summary, quantizes the gate and up
+ * projections with the other five; this entry point saves writing both
+ * projections' outputs and reading them back for the activation.
+ *
+ *   x        [M, K] bf16 bits, row-major
+ *   packed   [2F, K / 2] bytes and absmax [2F, K / 64] fp32: ONE weight
+ *            [2F, K] = the gate weight (rows 0 .. F-1) followed by the up
+ *            weight (rows F .. 2F-1), quantized by nf4_quantize as one tensor
+ *   F        the MLP's intermediate width (outputs per row)
+ *   y        [M, F] bf16 bits out, row-major; G in fp32, the activation and
+ *            the product in fp32, one bf16 rounding at the end
+ *   workspace, workspace_bytes  at least nf4_linear_workspace_size(M, 2F, K)
+ *            bytes (NULL allowed when that is 0)
+ *
+ * Requirements and errors as for nf4_linear with N = 2F (F < 2^30).  Not
+ * bit-exact: matches gelu_tanh(g) * u of an fp64 matmul of the dequantized
+ * weights to within fp32 summation error, the fp32 activation and one bf16
+ * rounding.
+ */
+NF4_API nf4_status nf4_linear_geglu(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                                    const float* absmax, int64_t F, int32_t block, uint16_t* y,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace nf4_linear needs for this shape (host only, no device
  * call).  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad arguments. */
 NF4_API nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);

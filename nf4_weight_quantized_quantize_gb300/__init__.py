@@ -3,12 +3,14 @@
 Two layers, both argument marshalling only -- every step of the computation
 runs in the library's CUDA kernels:
 
-* ``nf4_quantize``, ``nf4_dequantize``, ``nf4_linear``, ``nf4_linear_noalloc``,
-  ``nf4_linear_workspace_size``, ``nf4_last_error``, ``nf4_status_string``:
+* ``nf4_quantize``, ``nf4_dequantize``, ``nf4_linear``, ``nf4_linear_geglu``,
+  ``nf4_linear_noalloc``, ``nf4_linear_workspace_size``, ``nf4_last_error``,
+  ``nf4_status_string``:
   the C entry points of ``include/nf4.h`` under the same names, taking plain
   integers (device addresses, sizes, a stream handle) and returning the
   status code.
-* ``quantize``, ``dequantize``, ``linear``: the same calls on torch tensors.
+* ``quantize``, ``dequantize``, ``linear``, ``linear_geglu``: the same calls on
+  torch tensors.
   They check dtypes and devices, allocate the outputs with torch, pass the raw
   pointers and the current stream, and raise :class:`NF4Error` on a nonzero
   status.
@@ -53,6 +55,7 @@ def _load():
         "nf4_version": [],
         "nf4_launch_count": [],
         "nf4_linear_noalloc": [P, I64, I64, P, P, I64, I32, P, P],
+        "nf4_linear_geglu": [P, I64, I64, P, P, I64, I32, P, P, SZ, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -94,6 +97,11 @@ def nf4_dequantize(packed: int, absmax: int, numel: int, block: int, out: int, s
 def nf4_linear(x: int, M: int, K: int, packed: int, absmax: int, N: int, block: int, y: int,
                workspace: int, workspace_bytes: int, stream: int = 0) -> int:
     return lib().nf4_linear(x, M, K, packed, absmax, N, block, y, workspace, workspace_bytes, stream)
+
+
+def nf4_linear_geglu(x: int, M: int, K: int, packed: int, absmax: int, F: int, block: int, y: int,
+                     workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return lib().nf4_linear_geglu(x, M, K, packed, absmax, F, block, y, workspace, workspace_bytes, stream)
 
 
 def nf4_linear_noalloc(x: int, M: int, K: int, packed: int, absmax: int, N: int, block: int, y: int,
@@ -202,4 +210,29 @@ def linear(x, packed, absmax, n_out: int, out=None, workspace=None):
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(nf4_linear(x.data_ptr(), M, K, packed.data_ptr(), absmax.data_ptr(), n_out, BLOCK,
                       out.data_ptr(), ws_ptr, ws_len, _stream(x.device)), "nf4_linear")
+    return out
+
+
+def linear_geglu(x, packed, absmax, n_ff: int, out=None, workspace=None):
+    """Y [M, n_ff] bf16 = gelu_tanh(X . Wg^T) * (X . Wu^T), where (packed, absmax)
+    is ONE NF4 weight [2 n_ff, K]: the gate rows, then the up rows."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _need(packed, torch.uint8, "packed")
+    _need(absmax, torch.float32, "absmax")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    if packed.numel() * 2 != 2 * n_ff * K or absmax.numel() * BLOCK != 2 * n_ff * K:
+        raise ValueError("packed/absmax do not match [2 n_ff, K]")
+    if out is None:
+        out = torch.empty(M, n_ff, dtype=torch.bfloat16, device=x.device)
+    st, ws_bytes = nf4_linear_workspace_size(M, 2 * n_ff, K)
+    _check(st, "nf4_linear_workspace_size")
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(nf4_linear_geglu(x.data_ptr(), M, K, packed.data_ptr(), absmax.data_ptr(), n_ff, BLOCK,
+                            out.data_ptr(), ws_ptr, ws_len, _stream(x.device)), "nf4_linear_geglu")
     return out

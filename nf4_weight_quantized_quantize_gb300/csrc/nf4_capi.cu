@@ -136,6 +136,32 @@ nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* pa
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 
+nf4_status nf4_linear_geglu(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                            const float* absmax, int64_t F, int32_t block, uint16_t* y, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
+    if (M < 0 || F < 0 || K <= 0 || K % NF4_BLOCK != 0) return NF4_ERR_SHAPE;
+    // TMA coordinates are 32-bit: keep every extent (2F rows of weight) below 2^31.
+    if (M >= (int64_t(1) << 31) || F >= (int64_t(1) << 30) || K >= (int64_t(1) << 31)) return NF4_ERR_SHAPE;
+    if (M == 0 || F == 0) return NF4_OK;
+    if (!x || !packed || !absmax || !y) return NF4_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 16) || !aligned(absmax, 4))
+        return NF4_ERR_ALIGN;
+    size_t need = 0;
+    nf4_linear_workspace_size(M, 2 * F, K, &need);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return NF4_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return NF4_ERR_ALIGN;
+    }
+    const nf4::DeviceInfo* dev = nullptr;
+    if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = (M >= 128) ? nf4::launch_gemm_geglu(*dev, x, M, K, packed, absmax, F, y, s)
+                               : nf4::launch_skinny(*dev, x, M, K, packed, absmax, 2 * F, y, workspace,
+                                                    workspace_bytes, s, true);
+    return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+
 nf4_status nf4_last_error(void* stream) {
     const nf4::DeviceInfo* dev = nullptr;
     if (nf4_status st = current_device(&dev); st != NF4_OK) return st;

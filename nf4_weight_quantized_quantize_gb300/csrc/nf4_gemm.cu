@@ -10,12 +10,16 @@
 // weight crosses HBM at 0.5625 bytes per element and never touches shared
 // memory in bf16 form.
 //
-// One kernel template, two uses:
+// One kernel template, three uses:
 //   direct (M >= 128): CTA tile = 128 weight rows x NX activation rows
 //       (NX <= 256), the whole K range, bf16 Y written by the epilogue.
 //   split (M < 128):  NX = M rounded up to 16, K split over CTAs so every SM
 //       streams weights; fp32 partials to a workspace, then an ordered
 //       reduction kernel writes bf16 Y.
+//   gate/up pair (GEGLU, M >= 128): the weight is the Gemma3 MLP's gate and
+//       up projections stacked into one [2F, K] tensor; a tile's 128 rows are
+//       64 gate rows and the 64 up rows of the same outputs, and the epilogue
+//       writes gelu_tanh(gate) * up, [M, F], instead of both projections.
 //
 // The MMA runs "swap-AB": the converted weight tile is operand A (M = 128,
 // in TMEM), the activation tile is operand B (N = NX, in shared memory, 128-byte
@@ -203,31 +207,64 @@ __device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint3
 }
 
 // Weight producer warp, one stage: lane 0 arms pfull[p] with the TMA byte
-// count and loads the packed tile of the whole stage (one box of 32 * KS
-// bytes x ROWS rows); every lane copies scales with 4-byte cp.async --
-// K-slice h, rows lane, lane + 32, ... to am_dst[h][row] -- and arrives on
-// pfull[p] when its copies land.  Rows past N and K-slices past the weight's
-// last block copy a harmless in-range scale (their products are never
-// stored or multiply zeros).
-template <int ROWS, int KS>
+// count and loads the packed tile of the whole stage -- one box of 32 * KS
+// bytes x ROWS rows from weight row n0, or, for a gate/up PAIR, two boxes of
+// ROWS / 2 rows from rows n0 (gate) and n1 (up) -- and every lane copies
+// scales with 4-byte cp.async -- K-slice h, rows lane, lane + 32, ... to
+// am_dst[h][row] -- and arrives on pfull[p] when its copies land.  Rows of a
+// box at or past n_lim (the rows of one half) and K-slices past the weight's
+// last block copy a harmless in-range scale (their products are never stored
+// or multiply zeros).
+template <int ROWS, int KS, bool PAIR>
 __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_t tx_bytes, const CUtensorMap* tm_w,
-                                                uint32_t p_dst, int p_col0, int n0, uint32_t am_dst,
-                                                const float* absmax, int N, int am_pitch, int kb_abs0) {
+                                                uint32_t p_dst, int p_col0, int n0, int n1, int n_lim,
+                                                uint32_t am_dst, const float* absmax, int am_pitch, int kb_abs0) {
+    constexpr int H = PAIR ? ROWS / 2 : ROWS;   // rows per box
     if (lane == 0) {
         mbar_arrive_expect_tx(full, tx_bytes);
         tma_load_2d(p_dst, tm_w, full, p_col0, n0);
+        if constexpr (PAIR) tma_load_2d(p_dst + H * kPackedRow * KS, tm_w, full, p_col0, n1);
     }
 #pragma unroll
     for (int h = 0; h < KS; ++h) {
         const bool kb_ok = kb_abs0 + h < am_pitch;
 #pragma unroll
         for (int i = lane; i < ROWS; i += 32) {
-            const int n = n0 + i;
-            const float* src = absmax + (n < N && kb_ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0);
+            const int il = i < H ? i : i - H;          // row within its box
+            const int n = (i < H ? n0 : n1) + il;
+            const bool ok = n0 + il < n_lim && kb_ok;
+            const float* src = absmax + (ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0);
             cp_async_4(am_dst + 4u * (h * ROWS + i), src);
         }
     }
     cp_async_arrive_noinc(full);
+}
+
+// GELU, tanh form (Hendrycks and Gimpel, "Gaussian Error Linear Units",
+// section 2), in fp32: x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float k = 0.7978845608028654f;   // sqrt(2 / pi)
+    return 0.5f * x * (1.0f + tanhf(k * fmaf(0.044715f * x, x * x, x)));
+}
+
+// Named barriers among the converter warps (barrier 0 is __syncthreads).
+// and_all: every converter thread arrives, each with its predicate; returns
+// whether all of them were true.
+__device__ __forceinline__ bool converters_and_all(bool pred, int threads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void converters_sync(int threads) {
+    asm volatile("bar.sync 2, %0;" ::"r"(threads) : "memory");
 }
 
 // ============================================================ the kernel
@@ -311,20 +348,25 @@ struct TsCfg {
 };
 
 struct TsArgs {
-    const float* absmax;  // [N, K/64]
-    uint16_t* y;          // [M, N] (direct)
+    const float* absmax;  // [N, K/64] ([2N, K/64] for a gate/up pair)
+    uint16_t* y;          // [M, N] (direct, gate/up pair)
     float* ws;            // [splits, M, N] fp32 partials (split)
-    int M, N, K;
+    int M, N, K;          // N: output columns (rows of one half of a gate/up pair)
     int kb_per_split;
     int m_tiles;
     uint32_t* err;
 };
 
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT>
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU>
 __global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
     using C = TsCfg<NX, KS, RS, LUT, WS>;
+    static_assert(!(SPLIT && GEGLU), "a gate/up pair sums its split-K partials before the activation");
+    // output columns per tile: 128 weight rows, or 64 gate/up row pairs
+    constexpr int HW = GEGLU ? C::BW / 2 : C::BW;
+    // the up half's accumulators go through the (idle) activation ring
+    static_assert(!GEGLU || C::SX * C::X_SLOT >= NX * HW * 4, "gate/up exchange buffer");
     constexpr int SX = C::SX;
     constexpr int ST = C::ST;
     constexpr int SP = C::SP;
@@ -343,7 +385,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int lane = threadIdx.x & 31;
     // tiles run m-fastest: CTAs resident together share each weight tile through L2
     const int m0 = static_cast<int>(blockIdx.x % args.m_tiles) * NX;
-    const int n0 = static_cast<int>(blockIdx.x / args.m_tiles) * C::BW;
+    const int n0 = static_cast<int>(blockIdx.x / args.m_tiles) * HW;
     const int split = blockIdx.y;
     const int nk_total = args.K / kBK;
     const int kb0 = split * args.kb_per_split;
@@ -414,9 +456,9 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 ok = mbar_wait(bar.done(prev % ST), (prev / ST) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             const int kb = kb0 + ws * C::WK;
-            produce_weights<C::BW, C::WK>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
-                                          kb * kPackedRow, n0, smem_u32(am_tile(p)), args.absmax, args.N, nk_total,
-                                          kb);
+            produce_weights<C::BW, C::WK, GEGLU>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
+                                                 kb * kPackedRow, n0, args.N + n0, args.N, smem_u32(am_tile(p)),
+                                                 args.absmax, nk_total, kb);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(bar.pfull(0), SP, issued, args.err);
@@ -550,7 +592,64 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
-        if (__all_sync(0xffffffffu, ok)) {
+        // accumulators of an issuer that had no K-slice were never written
+        const int nacc = min(C::MI, min(KS, nk)) * C::ACC_PER_MI;
+        // sum of the NACC accumulators of this lane's row at columns c0 .. c0 + 15
+        auto load_acc = [&](int c0, uint32_t (&v)[16]) {
+            tmem_ld16(lane_addr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int a = 1; a < C::NACC; ++a) {
+                if (a >= nacc) break;
+                uint32_t w[16];
+                tmem_ld16(lane_addr + a * C::ACC_STRIDE + c0, w);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+            }
+        };
+        if constexpr (GEGLU) {
+            // Lanes 0-63 hold the gate rows n0 + r, lanes 64-127 the up rows of
+            // the same outputs.  The gate warps put gelu(gate) in shared memory
+            // (the activation ring: every load into it was read by an MMA that
+            // has completed), the up warps multiply it in and write Y.  Every
+            // converter thread reaches both barriers whatever happened before.
+            constexpr int kConvThreads = 32 * C::CONV_WARPS;
+            const bool all_ok = converters_and_all(__all_sync(0xffffffffu, ok), kConvThreads);
+            float* gbuf = reinterpret_cast<float*>(smem);   // [NX][64]: column c, row r at c * 64 + r
+            if (all_ok) {
+                tc_fence_after();
+                fence_proxy_async_smem();   // the ring was last written by TMA, read by the MMAs
+                if (q < 2) {
+#pragma unroll 1
+                    for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
+                        uint32_t v[16];
+                        load_acc(c0, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) gbuf[(c0 + i) * HW + r] = gelu_tanh(__uint_as_float(v[i]));
+                    }
+                }
+            }
+            converters_sync(kConvThreads);
+            if (all_ok && q >= 2) {
+                const int rr = r - HW;
+                const int n = n0 + rr;
+#pragma unroll 1
+                for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
+                    uint32_t v[16];
+                    load_acc(c0, v);
+                    if (n < args.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = m0 + c0 + i;
+                            if (m < args.M)
+                                args.y[static_cast<int64_t>(m) * args.N + n] = __bfloat16_as_ushort(
+                                    __float2bfloat16_rn(gbuf[(c0 + i) * HW + rr] * __uint_as_float(v[i])));
+                        }
+                    }
+                }
+            }
+        } else if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             // accumulator: TMEM lane = weight row n, column c = activation row m0 + c;
             // 16-column chunks go round-robin over the KS * RS warps of each lane quarter
@@ -558,19 +657,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 #pragma unroll 1
             for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
                 uint32_t v[16];
-                tmem_ld16(lane_addr + c0, v);
-                tmem_ld_wait();
-                // accumulators of an issuer that had no K-slice were never written
-                const int nacc = min(C::MI, min(KS, nk)) * C::ACC_PER_MI;
-#pragma unroll
-                for (int a = 1; a < C::NACC; ++a) {
-                    if (a >= nacc) break;
-                    uint32_t w[16];
-                    tmem_ld16(lane_addr + a * C::ACC_STRIDE + c0, w);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
-                }
+                load_acc(c0, v);
                 if (n < args.N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -607,6 +694,27 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
         float acc = ws[i];
         for (int s = 1; s < splits; ++s) acc += ws[static_cast<int64_t>(s) * mn + i];
         y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+    }
+}
+
+// Gate/up pair, M < 128: the split-K partials cover all 2F rows
+// ([splits, M, 2F]); sum the gate and the up partials in split order, then
+// write bf16(gelu(gate) * up), [M, F].
+__global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t F,
+                                           uint16_t* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t mn2 = M * 2 * F;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * F;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / F, n = i - m * F;
+        const float* g = ws + m * 2 * F + n;
+        float gs = g[0], us = g[F];
+        for (int s = 1; s < splits; ++s) {
+            gs += g[s * mn2];
+            us += g[s * mn2 + F];
+        }
+        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(gs) * us));
     }
 }
 
@@ -726,12 +834,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT>
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
     using C = TsCfg<NX, KS, RS, LUT, WS>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT>;
+    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT, GEGLU>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -743,40 +851,43 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS, int LUT, int WS>
+template <bool SPLIT, int KS, int RS, int LUT, int WS, bool GEGLU>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
 }
 
-cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x, int64_t M, int64_t K,
+// N: rows of the weight.  pair: the weight is a gate/up pair ([2F, K], N = 2F)
+// and the GEGLU epilogue writes [M, F] (direct path only).
+cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const uint16_t* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, float* ws,
                         cudaStream_t s) {
+    if (pair && (p.split || N % 2 != 0)) return cudaErrorInvalidValue;
     CUtensorMap tm_x, tm_w;
     const int ks = p.split ? kKsSplit * kWsSplit : kKsDirect * kWsDirect;   // K-slices per weight slot
     // the packed box row is 32 * ks bytes; its swizzle span matches (TsCfg::packed_offset)
@@ -784,12 +895,14 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, const uint16_t* x,
                                  : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
                                            : CU_TENSOR_MAP_SWIZZLE_128B;
     if (!make_map(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, p.nx, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, kBW, kPackedRow * ks, wsw))
+        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, pair ? kBW / 2 : kBW,
+                  kPackedRow * ks, wsw))
         return cudaErrorInvalidValue;
-    TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.kb_per_split,
-             p.m_tiles, dev.err_word};
-    return p.split ? dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit>(dev, p, tm_x, tm_w, a, s)
-                   : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect>(dev, p, tm_x, tm_w, a, s);
+    TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(pair ? N / 2 : N), static_cast<int>(K),
+             p.kb_per_split, p.m_tiles, dev.err_word};
+    if (p.split) return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false>(dev, p, tm_x, tm_w, a, s);
+    return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true>(dev, p, tm_x, tm_w, a, s)
+                : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false>(dev, p, tm_x, tm_w, a, s);
 }
 
 }  // namespace
@@ -798,7 +911,15 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int
                         const float* absmax, int64_t N, uint16_t* y, cudaStream_t s) {
     const Plan p = make_plan(M, N, K);
     if (p.split) return cudaErrorInvalidValue;
-    return launch_plan(dev, p, x, M, K, packed, absmax, N, y, nullptr, s);
+    return launch_plan(dev, p, false, x, M, K, packed, absmax, N, y, nullptr, s);
+}
+
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                              const float* absmax, int64_t F, uint16_t* y, cudaStream_t s) {
+    // ceil(2F / 128) tiles of 128 weight rows = ceil(F / 64) tiles of 64 gate/up row pairs
+    const Plan p = make_plan(M, 2 * F, K);
+    if (p.split) return cudaErrorInvalidValue;
+    return launch_plan(dev, p, true, x, M, K, packed, absmax, 2 * F, y, nullptr, s);
 }
 
 size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K) {
@@ -806,21 +927,24 @@ size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K
     return static_cast<size_t>(p.splits) * M * N * sizeof(float);
 }
 
+// N: rows of the weight; geglu: the weight is a gate/up pair (N = 2F) and
+// the reduction writes gelu(gate) * up, [M, F].
 cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
                           const float* absmax, int64_t N, uint16_t* y, void* workspace, size_t ws_bytes,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool geglu) {
     const Plan p = make_plan(M, N, K);
-    if (!p.split || ws_bytes < skinny_workspace_bytes(&dev, M, N, K)) return cudaErrorInvalidValue;
-    if (cudaError_t e = launch_plan(dev, p, x, M, K, packed, absmax, N, y, static_cast<float*>(workspace), s);
+    if (!p.split || ws_bytes < skinny_workspace_bytes(&dev, M, N, K) || (geglu && N % 2 != 0))
+        return cudaErrorInvalidValue;
+    if (cudaError_t e = launch_plan(dev, p, false, x, M, K, packed, absmax, N, y, static_cast<float*>(workspace), s);
         e != cudaSuccess)
         return e;
-    const int64_t mn = M * N;
+    const int64_t mn = geglu ? M * (N / 2) : M * N;   // outputs
     const int threads = 256;
     const int grid = static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
-    if (cudaError_t e = launch_pdl(splitk_reduce_kernel, grid, threads, 0, s, static_cast<const float*>(workspace),
-                                   p.splits, mn, y);
-        e != cudaSuccess)
-        return e;
+    const float* wsf = static_cast<const float*>(workspace);
+    cudaError_t e = geglu ? launch_pdl(splitk_geglu_reduce_kernel, grid, threads, 0, s, wsf, p.splits, M, N / 2, y)
+                          : launch_pdl(splitk_reduce_kernel, grid, threads, 0, s, wsf, p.splits, mn, y);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -61,10 +61,17 @@ cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int
 // Workspace bytes the skinny (M < 128) path needs for this shape.
 size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K);
 
+// Fused NF4 GEMM of a gate/up pair ([2F, K] weight, gate rows first) with the
+// GELU-gated product as epilogue, M >= 128: y [M, F] = gelu(X Wg^T) * (X Wu^T).
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+                              const uint8_t* packed, const float* absmax, int64_t F, uint16_t* y,
+                              cudaStream_t s);
+
 // Skinny path: swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an
-// ordered reduction.
+// ordered reduction.  N is the weight's row count; with geglu the weight is a
+// gate/up pair (N = 2F) and the reduction writes gelu(gate) * up, [M, F].
 cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
                           const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
-                          void* workspace, size_t ws_bytes, cudaStream_t s);
+                          void* workspace, size_t ws_bytes, cudaStream_t s, bool geglu = false);
 
 }  // namespace nf4

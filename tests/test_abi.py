@@ -112,6 +112,30 @@ def test_linear_argument_errors():
         assert call(M=16, N=3840, K=15360, workspace=FAKE + 4, workspace_bytes=need) == nf4.NF4_ERR_ALIGN
 
 
+def test_linear_geglu_argument_errors():
+    ok = dict(x=FAKE, M=256, K=128, packed=FAKE, absmax=FAKE, F=64, block=64, y=FAKE,
+              workspace=0, workspace_bytes=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return nf4.nf4_linear_geglu(a["x"], a["M"], a["K"], a["packed"], a["absmax"], a["F"], a["block"],
+                                    a["y"], a["workspace"], a["workspace_bytes"])
+
+    assert call(block=32) == nf4.NF4_ERR_BLOCKSIZE
+    assert call(K=100) == nf4.NF4_ERR_SHAPE
+    assert call(F=-1) == nf4.NF4_ERR_SHAPE
+    assert call(F=1 << 30) == nf4.NF4_ERR_SHAPE          # 2F weight rows must stay below 2^31
+    assert call(x=0) == nf4.NF4_ERR_NULL
+    assert call(y=0) == nf4.NF4_ERR_NULL
+    assert call(y=FAKE + 2) == nf4.NF4_ERR_ALIGN
+    assert call(M=0) == nf4.NF4_OK and call(F=0) == nf4.NF4_OK
+    # the skinny path's workspace is that of the [2F, K] weight
+    _, need = nf4.nf4_linear_workspace_size(16, 2 * 15360, 3840)
+    assert need > 0
+    assert call(M=16, F=15360, K=3840) == nf4.NF4_ERR_WORKSPACE
+    assert call(M=16, F=15360, K=3840, workspace=FAKE, workspace_bytes=need - 1) == nf4.NF4_ERR_WORKSPACE
+
+
 def test_workspace_size_rules():
     assert nf4.nf4_linear_workspace_size(2048, 4096, 3840) == (nf4.NF4_OK, 0)
     assert nf4.nf4_linear_workspace_size(16, 4096, 100)[0] == nf4.NF4_ERR_SHAPE
