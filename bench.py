@@ -460,12 +460,70 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }
+    if not args.no_geglu:
+        line["geglu"] = geglu_block(dev)
     if not args.no_stack:
         line["stack"] = stack_block(dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))
     return 0
+
+
+def geglu_block(dev, reps: int = 20):
+    """The Gemma3 MLP's gate and up projections as one fused call
+    (nf4_linear_geglu: [2F, K] NF4 weight, gelu_tanh(gate) * up written as
+    [M, F]) against nf4_linear over the same stacked weight (both projections'
+    outputs written, [M, 2F], the activation left to another kernel), at
+    M = 2048 and M = 16.  Mean of `reps` calls, L2 flushed before each."""
+    import torch
+    import nf4_weight_quantized_quantize_gb300 as nf4
+
+    cfg = workloads.GATE_UP
+    F = cfg.n // 2
+    stream = torch.cuda.current_stream(dev)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    w = workloads.make_weight(cfg, device=dev)
+    p, a = nf4.quantize(w)
+    del w
+    x = workloads.make_activation(cfg, device=dev)
+    xs = x[:SKINNY_M].contiguous()
+    y2 = torch.empty(cfg.m, 2 * F, dtype=torch.bfloat16, device=dev)
+    y1 = torch.empty(cfg.m, F, dtype=torch.bfloat16, device=dev)
+    _, wsb = nf4.nf4_linear_workspace_size(SKINNY_M, 2 * F, cfg.k)
+    wsp = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        ev = [(mk(), mk()) for _ in range(reps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    t_fused = timed(lambda: nf4.linear_geglu(x, p, a, F, out=y1))
+    t_plain = timed(lambda: nf4.linear(x, p, a, 2 * F, out=y2))
+    t_fused_s = timed(lambda: nf4.linear_geglu(xs, p, a, F, out=y1[:SKINNY_M], workspace=wsp))
+    t_plain_s = timed(lambda: nf4.linear(xs, p, a, 2 * F, out=y2[:SKINNY_M], workspace=wsp))
+    if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
+        raise RuntimeError("a kernel reported a timeout in the gate/up measurement")
+    pk, _ = peaks()
+    flop = 2 * cfg.m * 2 * F * cfg.k
+    tf = lambda ms: flop / (ms * 1e-3) / 1e12  # noqa: E731
+    del p, a, x, xs, y1, y2, wsp, flush
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"gemma3_12b_gate_up_pair_F{F}_K{cfg.k}",
+        "m2048": {"fused_ms": t_fused, "fused_TFLOP/s": tf(t_fused), "frac_bf16": tf(t_fused) / pk["bf16_tflops"],
+                  "unfused_linear_ms": t_plain, "unfused_linear_TFLOP/s": tf(t_plain),
+                  "output_bytes_fused": cfg.m * F * 2, "output_bytes_unfused": cfg.m * 2 * F * 2},
+        "m16": {"fused_ms": t_fused_s, "unfused_linear_ms": t_plain_s},
+        "timing": f"mean of {reps} calls, CUDA events, 512 MiB L2 flush before each",
+    }
 
 
 def stack_block(dev, passes: int = 2):
@@ -566,6 +624,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="omit the CPU oracle timing")
     ap.add_argument("--no-stack", action="store_true", help="omit the 48-layer stack measurement")
+    ap.add_argument("--no-geglu", action="store_true", help="omit the fused gate/up measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

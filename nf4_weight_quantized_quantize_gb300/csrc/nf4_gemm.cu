@@ -241,10 +241,20 @@ __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_
 }
 
 // GELU, tanh form (Hendrycks and Gimpel, "Gaussian Error Linear Units",
-// section 2), in fp32: x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))).
+// section 2): x/2 * (1 + tanh(y)), y = sqrt(2/pi) * (x + 0.044715 x^3), in
+// fp32 through the identity (1 + tanh(y)) / 2 = 1 / (1 + e^(-2y)):
+//   gelu(x) = x / (1 + 2^(x (c0 + c1 x^2))),  c0 = -2 sqrt(2/pi) log2(e),
+//   c1 = 0.044715 c0,
+// with the hardware base-2 exponential and reciprocal (a few 1e-7 relative
+// error; no cancellation, the denominator is at least 1).  For large negative
+// x the power overflows to +inf, its reciprocal is 0 and the result -0, the
+// limit.
 __device__ __forceinline__ float gelu_tanh(float x) {
-    const float k = 0.7978845608028654f;   // sqrt(2 / pi)
-    return 0.5f * x * (1.0f + tanhf(k * fmaf(0.044715f * x, x * x, x)));
+    const float a = x * fmaf(-0.10294324159622192f, x * x, -2.302208185195923f);
+    float t, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(a));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+    return x * r;
 }
 
 // Named barriers among the converter warps (barrier 0 is __syncthreads).
@@ -610,41 +620,49 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         };
         if constexpr (GEGLU) {
             // Lanes 0-63 hold the gate rows n0 + r, lanes 64-127 the up rows of
-            // the same outputs.  The gate warps put gelu(gate) in shared memory
-            // (the activation ring: every load into it was read by an MMA that
-            // has completed), the up warps multiply it in and write Y.  Every
-            // converter thread reaches both barriers whatever happened before.
+            // the same outputs.  A warp's 16-column chunks alternate between
+            // its two halves of the work: the gate warps write the even chunks
+            // of Y and the up warps the odd ones.  First each side parks its
+            // raw accumulators of the chunks the other side writes in shared
+            // memory (the activation ring: every load into it was read by an
+            // MMA that has completed); then each side finishes its own chunks
+            // with the other's values.  Every converter thread reaches both
+            // barriers whatever happened before.
             constexpr int kConvThreads = 32 * C::CONV_WARPS;
+            constexpr int kStride = 16 * KS * RS;           // between a warp's chunks
             const bool all_ok = converters_and_all(__all_sync(0xffffffffu, ok), kConvThreads);
-            float* gbuf = reinterpret_cast<float*>(smem);   // [NX][64]: column c, row r at c * 64 + r
+            float* xbuf = reinterpret_cast<float*>(smem);   // [NX][64]: column c, pair row rr at c * 64 + rr
+            const bool gate = q < 2;
+            const int rr = gate ? r : r - HW;               // row within the 64 pairs
             if (all_ok) {
                 tc_fence_after();
                 fence_proxy_async_smem();   // the ring was last written by TMA, read by the MMAs
-                if (q < 2) {
 #pragma unroll 1
-                    for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
-                        uint32_t v[16];
-                        load_acc(c0, v);
+                for (int c0 = 16 * u + (gate ? kStride : 0); c0 < NX; c0 += 2 * kStride) {
+                    uint32_t v[16];
+                    load_acc(c0, v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) gbuf[(c0 + i) * HW + r] = gelu_tanh(__uint_as_float(v[i]));
-                    }
+                    for (int i = 0; i < 16; ++i) xbuf[(c0 + i) * HW + rr] = __uint_as_float(v[i]);
                 }
             }
             converters_sync(kConvThreads);
-            if (all_ok && q >= 2) {
-                const int rr = r - HW;
+            if (all_ok) {
                 const int n = n0 + rr;
 #pragma unroll 1
-                for (int c0 = 16 * u; c0 < NX; c0 += 16 * KS * RS) {
+                for (int c0 = 16 * u + (gate ? 0 : kStride); c0 < NX; c0 += 2 * kStride) {
                     uint32_t v[16];
                     load_acc(c0, v);
                     if (n < args.N) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int m = m0 + c0 + i;
+                            const float mine = __uint_as_float(v[i]);
+                            const float other = xbuf[(c0 + i) * HW + rr];
+                            const float g = gate ? mine : other;
+                            const float up = gate ? other : mine;
                             if (m < args.M)
-                                args.y[static_cast<int64_t>(m) * args.N + n] = __bfloat16_as_ushort(
-                                    __float2bfloat16_rn(gbuf[(c0 + i) * HW + rr] * __uint_as_float(v[i])));
+                                args.y[static_cast<int64_t>(m) * args.N + n] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(g) * up));
                         }
                     }
                 }

@@ -3,7 +3,8 @@
     python -m nf4_weight_quantized_quantize_gb300.run_case \
         --workload gemma3_12b_gate_up_m2048 --op linear --iters 3
 
---op is one of quantize, dequantize, linear.  The workloads are the seeded
+--op is one of quantize, dequantize, linear, linear_geglu (the workload's
+weight read as a stacked gate/up pair, F = N / 2).  The workloads are the seeded
 Gemma3-12B projection shapes of workloads.py; inputs are generated on the
 device.  Prints the median CUDA-event time of the calls.
 """
@@ -29,7 +30,7 @@ def main(argv=None):
                                  workloads.DOWN_SKINNY)}
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", choices=sorted(cases), default=workloads.GATE_UP.name)
-    ap.add_argument("--op", choices=["quantize", "dequantize", "linear"], default="linear")
+    ap.add_argument("--op", choices=["quantize", "dequantize", "linear", "linear_geglu"], default="linear")
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args(argv)
     cfg = cases[a.workload]
@@ -41,6 +42,12 @@ def main(argv=None):
     elif a.op == "dequantize":
         out = torch.empty(w.numel(), dtype=torch.bfloat16, device=dev)
         fn = lambda: nf4.dequantize(packed, absmax, w.numel(), out=out)  # noqa: E731
+    elif a.op == "linear_geglu":
+        x = workloads.make_activation(cfg, device=dev)
+        y = torch.empty(cfg.m, cfg.n // 2, dtype=torch.bfloat16, device=dev)
+        _, wsb = nf4.nf4_linear_workspace_size(cfg.m, cfg.n, cfg.k)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        fn = lambda: nf4.linear_geglu(x, packed, absmax, cfg.n // 2, out=y, workspace=ws)  # noqa: E731
     else:
         x = workloads.make_activation(cfg, device=dev)
         y = torch.empty(cfg.m, cfg.n, dtype=torch.bfloat16, device=dev)
