@@ -440,3 +440,150 @@ def test_linear_geglu_brute_force_small():
     # swapping the halves gives a different answer on this case
     swapped = [[gelu(dot(m, F + n)) * dot(m, n) for n in range(F)] for m in range(M)]
     assert np.max(np.abs(y - np.array(swapped))) > 1e-3
+
+
+# ---------------------------------------------------------------- fp16 and fp32 compute dtypes
+
+
+def f16_bits_of(values):
+    """binary16 bit patterns by numpy's fp32 -> fp16 cast (round to nearest even)."""
+    return np.asarray(values, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_f16_widening_matches_numpy_on_every_pattern():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_to_f32_array(h)
+    want = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def test_f16_rounding_matches_numpy():
+    """fp32 -> fp16 round to nearest even against numpy's cast: random bit
+    patterns over the whole fp32 range, every fp16 value and the midpoints
+    between neighbours (ties), the subnormal boundary and the overflow edge."""
+    rs = np.random.default_rng(17)
+    rand = rs.integers(0, 1 << 32, 400000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    rand = rand[np.isfinite(rand)]
+    f16 = np.arange(0, 0x7c00, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    mids = ((f16[:-1] + f16[1:]) / 2).astype(np.float32)            # exact in fp32: ties
+    edges = np.array([65504, 65519.996, 65520, 65536, 1e9, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                      2.0 ** -14, 2.0 ** -14 - 2.0 ** -25, 6e-8, 1e-30, 0.0], np.float32)
+    for v in (rand, mids, -mids, f16.astype(np.float32), edges, -edges):
+        got = oracle.f32_to_f16_array(v)
+        with np.errstate(over="ignore"):                 # numpy warns on values that round to inf
+            want = v.astype(np.float16).view(np.uint16)
+        assert np.array_equal(got, want)
+
+
+def test_dequant_f16_absmax_one_is_the_f16_codebook():
+    packed = np.arange(256, dtype=np.uint8)
+    absmax = np.ones(8, np.float32)
+    y = oracle.dequantize(packed, absmax, 512, dtype="f16")
+    cb16 = f16_bits_of(golden_codebook())
+    assert np.array_equal(y[0::2], cb16[packed >> 4]) and np.array_equal(y[1::2], cb16[packed & 15])
+
+
+def test_dequant_f16_and_f32_match_numpy_products():
+    """f16: numpy's fp16 of (fp32 of the fp16 codebook value) x absmax in fp32;
+    f32: the fp32 codebook value x absmax in fp32, no rounding to a smaller type."""
+    rs = np.random.default_rng(23)
+    n = 64 * 300
+    packed = rs.integers(0, 256, n // 2, dtype=np.uint16).astype(np.uint8)
+    absmax = np.abs(rs.standard_normal(n // 64) * 10.0 ** rs.integers(-6, 4, n // 64)).astype(np.float32)
+    absmax[::7] = f16_bits_of(absmax[::7]).view(np.float16).astype(np.float32)   # some fp16-exact scales
+    codes = np.empty(n, np.int64)
+    codes[0::2], codes[1::2] = packed >> 4, packed & 15
+    am = np.repeat(absmax, 64)
+    cb = golden_codebook()
+    c16 = cb.astype(np.float16).astype(np.float32)
+    want16 = (c16[codes] * am).astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.dequantize(packed, absmax, n, dtype="f16"), want16)
+    want32 = (cb[codes] * am).astype(np.float32)
+    assert np.array_equal(oracle.dequantize(packed, absmax, n, dtype="f32").view(np.uint32), want32.view(np.uint32))
+
+
+def _brute_quantize_values(w, block=BLOCK):
+    """Independent restatement on plain Python floats (the element values)."""
+    cb = [float(v) for v in golden_codebook()]
+    w = [float(v) for v in w]
+    codes, scales = [], []
+    for b0 in range(0, len(w), block):
+        blk = w[b0:b0 + block]
+        am = max(abs(v) for v in blk)
+        scales.append(am)
+        for v in blk:
+            if am == 0.0:
+                codes.append(7)
+                continue
+            n = float(np.float32(v) / np.float32(am))
+            dists = [abs(n - c) for c in cb]
+            codes.append(dists.index(min(dists)))
+    packed = bytes((codes[2 * j] << 4) | codes[2 * j + 1] for j in range(len(codes) // 2))
+    return np.frombuffer(packed, dtype=np.uint8), np.array(scales, dtype=np.float32)
+
+
+def test_quantize_f16_and_f32_brute_force():
+    wb = _special_weights()                               # bf16 patterns of special blocks
+    vals = f32_of_bits(wb)
+    rs = np.random.default_rng(29)
+    extra = (rs.standard_normal(64 * 6) * 0.03).astype(np.float32)
+    extra[64:128] *= 1e-6                                 # fp16 subnormal range
+    w32 = np.concatenate([vals, extra])
+    w16 = f16_bits_of(w32)
+    p, a = oracle.quantize(w16, dtype="f16")
+    bp, ba = _brute_quantize_values(w16.view(np.float16).astype(np.float32))
+    assert np.array_equal(p, bp) and np.array_equal(a.view(np.uint32), ba.view(np.uint32))
+    p, a = oracle.quantize(w32, dtype="f32")
+    bp, ba = _brute_quantize_values(w32)
+    assert np.array_equal(p, bp) and np.array_equal(a.view(np.uint32), ba.view(np.uint32))
+
+
+def test_quantize_is_dtype_blind_for_equal_values():
+    """The same values quantize identically whatever type carries them: bf16
+    and fp16 values widened exactly to fp32 give the bf16 / fp16 result."""
+    rs = np.random.default_rng(31)
+    v = (rs.standard_normal(64 * 40) * 0.02).astype(np.float32)
+    b16 = bf16_bits_of(v)
+    h16 = f16_bits_of(v)
+    pb, ab = oracle.quantize(b16)
+    assert all(np.array_equal(x, y) for x, y in zip((pb, ab), oracle.quantize(f32_of_bits(b16), dtype="f32")))
+    ph, ah = oracle.quantize(h16, dtype="f16")
+    assert all(np.array_equal(x, y) for x, y in
+               zip((ph, ah), oracle.quantize(h16.view(np.float16).astype(np.float32), dtype="f32")))
+
+
+def test_f16_round_trip_bound_and_exact_max():
+    rs = np.random.default_rng(37)
+    v = (rs.standard_normal(64 * 50) * 0.05).astype(np.float32)
+    w16 = f16_bits_of(v)
+    p, a = oracle.quantize(w16, dtype="f16")
+    y = oracle.dequantize(p, a, v.size, dtype="f16").view(np.float16).astype(np.float64)
+    w = w16.view(np.float16).astype(np.float64)
+    am = np.repeat(a.astype(np.float64), 64)
+    ulp = np.spacing(np.abs(y).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(w - y) <= (0.15190359950065613 + 2.0 ** -11) * am + ulp / 2 + 1e-12)
+    blocks = w.reshape(-1, 64)
+    idx = np.argmax(np.abs(blocks), axis=1)
+    ymax = y.reshape(-1, 64)[np.arange(blocks.shape[0]), idx]
+    assert np.array_equal(ymax, blocks[np.arange(blocks.shape[0]), idx])
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_linear_other_dtypes_brute_force(dtype):
+    rs = np.random.default_rng(41)
+    M, N, K = 3, 2, 128
+    wv = (rs.standard_normal(N * K) * 0.02).astype(np.float32)
+    xv = rs.standard_normal(M * K).astype(np.float32)
+    w = f16_bits_of(wv) if dtype == "f16" else wv
+    x = (f16_bits_of(xv) if dtype == "f16" else xv).reshape(M, K)
+    p, a = oracle.quantize(w, dtype=dtype)
+    y = oracle.linear(x, p, a, N, dtype=dtype)
+    wd = oracle.dequantize(p, a, N * K, dtype=dtype)
+    as_f = (lambda b: b.view(np.float16).astype(np.float64)) if dtype == "f16" else (lambda b: b.astype(np.float64))
+    wd, xf = [float(t) for t in as_f(wd)], [float(t) for t in as_f(x.ravel())]
+    for m in range(M):
+        for n in range(N):
+            terms = [xf[m * K + k] * wd[n * K + k] for k in range(K)]
+            assert abs(y[m, n] - math.fsum(terms)) <= 1e-13 * sum(abs(t) for t in terms)
