@@ -21,7 +21,14 @@
  *     its low nibble;
  *   - dequantized value = bf16_rne( float(bf16_rne(C[code])) * absmax ).
  *
- * bf16 tensors cross this interface as uint16_t bit patterns.
+ * The compute dtype (weights, activations, outputs) is bf16 in the plain
+ * entry points.  The _ex forms take an nf4_dtype: for fp16 every bf16 above
+ * reads binary16 (round to nearest even); for fp32 the dequantized value is
+ * C[code] * absmax in fp32 with no further rounding.  The packed format does
+ * not depend on the dtype: the same values quantize to the same bytes.
+ *
+ * bf16 and fp16 tensors cross this interface as 16-bit patterns (uint16_t),
+ * fp32 tensors as float.
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller (allocate
@@ -66,8 +73,16 @@ typedef enum nf4_status {
     NF4_ERR_WORKSPACE = 5,  /* workspace NULL or smaller than nf4_linear_workspace_size() */
     NF4_ERR_DEVICE = 6,     /* no current device, or it is not sm_103 */
     NF4_ERR_CUDA = 7,       /* a CUDA runtime call or launch failed */
-    NF4_ERR_TIMEOUT = 8     /* a kernel gave up on a bounded wait (reported by nf4_last_error) */
+    NF4_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by nf4_last_error) */
+    NF4_ERR_DTYPE = 9       /* an nf4_dtype this entry point does not take */
 } nf4_status;
+
+/* Compute dtypes of the _ex entry points. */
+typedef enum nf4_dtype {
+    NF4_DTYPE_BF16 = 0,
+    NF4_DTYPE_F16 = 1,
+    NF4_DTYPE_F32 = 2
+} nf4_dtype;
 
 /* The only block size supported. */
 #define NF4_BLOCK 64
@@ -157,6 +172,38 @@ NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uin
 NF4_API nf4_status nf4_linear_geglu(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
                                     const float* absmax, int64_t F, int32_t block, uint16_t* y,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same operations at another compute dtype.
+ * Page: "Gemma3 NF4 on GPU" (#39), Summary: the tensors that are not
+ * quantized stay in the compute dtype, whatever it is.
+ *
+ * nf4_quantize_ex    w is [numel] of `dtype` (bf16, fp16 or fp32); alignment
+ *                    as nf4_quantize with "16-byte aligned w" for the fast
+ *                    kernel; w must be aligned to its element size.
+ * nf4_dequantize_ex  out is [numel] of `dtype`; fp32 output is
+ *                    C[code] * absmax in fp32 (4 bytes per element written).
+ * nf4_linear_ex,     x and y of `dtype`, bf16 or fp16 (the MMA's operand
+ * nf4_linear_geglu_ex  types); fp32 returns NF4_ERR_DTYPE.  For fp16 the
+ *                    fused kernels scale fp16 codebook values by the absmax
+ *                    rounded to fp16, so they reproduce nf4_dequantize_ex's
+ *                    fp16 values exactly when every absmax is an fp16 value
+ *                    (true for weights nf4_quantize_ex quantized from fp16).
+ *
+ * Results, requirements and errors otherwise as the bf16 forms; a dtype
+ * outside nf4_dtype returns NF4_ERR_DTYPE.
+ */
+NF4_API nf4_status nf4_quantize_ex(const void* w, nf4_dtype dtype, int64_t numel, int32_t block,
+                                   uint8_t* packed, float* absmax, void* stream);
+NF4_API nf4_status nf4_dequantize_ex(const uint8_t* packed, const float* absmax, int64_t numel,
+                                     int32_t block, nf4_dtype dtype, void* out, void* stream);
+NF4_API nf4_status nf4_linear_ex(const void* x, nf4_dtype dtype, int64_t M, int64_t K,
+                                 const uint8_t* packed, const float* absmax, int64_t N, int32_t block,
+                                 void* y, void* workspace, size_t workspace_bytes, void* stream);
+NF4_API nf4_status nf4_linear_geglu_ex(const void* x, nf4_dtype dtype, int64_t M, int64_t K,
+                                       const uint8_t* packed, const float* absmax, int64_t F,
+                                       int32_t block, void* y, void* workspace,
+                                       size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace nf4_linear needs for this shape (host only, no device
  * call).  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad arguments. */

@@ -75,32 +75,79 @@ void nf4::count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n),
 
 int nf4::current_device_info(const nf4::DeviceInfo** out) { return current_device(out); }
 
+namespace {
+
+bool valid_dtype(int dt) { return dt == NF4_DTYPE_BF16 || dt == NF4_DTYPE_F16 || dt == NF4_DTYPE_F32; }
+size_t elem_bytes(int dt) { return dt == NF4_DTYPE_F32 ? 4 : 2; }
+
+// Host-side checks of nf4_linear_ex / nf4_linear_geglu_ex over a weight of
+// `rows` rows; NF4_OK with *empty set when there is nothing to do.
+nf4_status check_linear(const void* x, int dtype, int64_t M, int64_t K, const uint8_t* packed, const float* absmax,
+                        int64_t rows, int32_t block, const void* y, void* workspace, size_t workspace_bytes,
+                        bool* empty) {
+    *empty = false;
+    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
+    if (!valid_dtype(dtype)) return NF4_ERR_DTYPE;
+    if (M < 0 || rows < 0 || K <= 0 || K % NF4_BLOCK != 0) return NF4_ERR_SHAPE;
+    // TMA coordinates are 32-bit: keep every extent below 2^31.
+    if (M >= (int64_t(1) << 31) || rows >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return NF4_ERR_SHAPE;
+    if (dtype == NF4_DTYPE_F32) return NF4_ERR_DTYPE;   // the tensor-core path takes bf16 and fp16
+    if (M == 0 || rows == 0) {
+        *empty = true;
+        return NF4_OK;
+    }
+    if (!x || !packed || !absmax || !y) return NF4_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 16) || !aligned(absmax, 4)) return NF4_ERR_ALIGN;
+    size_t need = 0;
+    nf4_linear_workspace_size(M, rows, K, &need);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return NF4_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return NF4_ERR_ALIGN;
+    }
+    return NF4_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
-nf4_status nf4_quantize(const uint16_t* w, int64_t numel, int32_t block, uint8_t* packed,
-                        float* absmax, void* stream) {
+nf4_status nf4_quantize_ex(const void* w, nf4_dtype dtype, int64_t numel, int32_t block, uint8_t* packed,
+                           float* absmax, void* stream) {
     if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
+    if (!valid_dtype(dtype)) return NF4_ERR_DTYPE;
     if (numel < 0 || numel % 2 != 0) return NF4_ERR_SHAPE;
     if (numel == 0) return NF4_OK;
     if (!w || !packed || !absmax) return NF4_ERR_NULL;
-    if (!aligned(w, 2) || !aligned(absmax, 4)) return NF4_ERR_ALIGN;
+    if (!aligned(w, elem_bytes(dtype)) || !aligned(absmax, 4)) return NF4_ERR_ALIGN;
     const nf4::DeviceInfo* dev = nullptr;
     if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
-    cudaError_t e = nf4::launch_quantize(*dev, w, numel, packed, absmax, static_cast<cudaStream_t>(stream));
+    cudaError_t e = nf4::launch_quantize(*dev, w, dtype, numel, packed, absmax, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+
+nf4_status nf4_quantize(const uint16_t* w, int64_t numel, int32_t block, uint8_t* packed,
+                        float* absmax, void* stream) {
+    return nf4_quantize_ex(w, NF4_DTYPE_BF16, numel, block, packed, absmax, stream);
+}
+
+nf4_status nf4_dequantize_ex(const uint8_t* packed, const float* absmax, int64_t numel, int32_t block,
+                             nf4_dtype dtype, void* out, void* stream) {
+    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
+    if (!valid_dtype(dtype)) return NF4_ERR_DTYPE;
+    if (numel < 0 || numel % 2 != 0) return NF4_ERR_SHAPE;
+    if (numel == 0) return NF4_OK;
+    if (!packed || !absmax || !out) return NF4_ERR_NULL;
+    if (!aligned(out, elem_bytes(dtype)) || !aligned(absmax, 4)) return NF4_ERR_ALIGN;
+    const nf4::DeviceInfo* dev = nullptr;
+    if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
+    cudaError_t e =
+        nf4::launch_dequantize(*dev, packed, absmax, numel, dtype, out, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 
 nf4_status nf4_dequantize(const uint8_t* packed, const float* absmax, int64_t numel, int32_t block,
                           uint16_t* out, void* stream) {
-    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
-    if (numel < 0 || numel % 2 != 0) return NF4_ERR_SHAPE;
-    if (numel == 0) return NF4_OK;
-    if (!packed || !absmax || !out) return NF4_ERR_NULL;
-    if (!aligned(out, 2) || !aligned(absmax, 4)) return NF4_ERR_ALIGN;
-    const nf4::DeviceInfo* dev = nullptr;
-    if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
-    cudaError_t e = nf4::launch_dequantize(*dev, packed, absmax, numel, out, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+    return nf4_dequantize_ex(packed, absmax, numel, block, NF4_DTYPE_BF16, out, stream);
 }
 
 nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
@@ -110,56 +157,55 @@ nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* by
     return NF4_OK;
 }
 
-nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
-                      const float* absmax, int64_t N, int32_t block, uint16_t* y, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
-    if (M < 0 || N < 0 || K <= 0 || K % NF4_BLOCK != 0) return NF4_ERR_SHAPE;
-    // TMA coordinates are 32-bit: keep every extent below 2^31.
-    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return NF4_ERR_SHAPE;
-    if (M == 0 || N == 0) return NF4_OK;
-    if (!x || !packed || !absmax || !y) return NF4_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 16) || !aligned(absmax, 4))
-        return NF4_ERR_ALIGN;
-    size_t need = 0;
-    nf4_linear_workspace_size(M, N, K, &need);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return NF4_ERR_WORKSPACE;
-        if (!aligned(workspace, 16)) return NF4_ERR_ALIGN;
-    }
+nf4_status nf4_linear_ex(const void* x, nf4_dtype dtype, int64_t M, int64_t K, const uint8_t* packed,
+                         const float* absmax, int64_t N, int32_t block, void* y, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    bool empty = false;
+    if (nf4_status st = check_linear(x, dtype, M, K, packed, absmax, N, block, y, workspace, workspace_bytes, &empty);
+        st != NF4_OK || empty)
+        return st;
     const nf4::DeviceInfo* dev = nullptr;
     if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = (M >= 128)
-                        ? nf4::launch_gemm(*dev, x, M, K, packed, absmax, N, y, s)
-                        : nf4::launch_skinny(*dev, x, M, K, packed, absmax, N, y, workspace, workspace_bytes, s);
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    uint16_t* ys = static_cast<uint16_t*>(y);
+    cudaError_t e = (M >= 128) ? nf4::launch_gemm(*dev, dtype, xs, M, K, packed, absmax, N, ys, s)
+                               : nf4::launch_skinny(*dev, dtype, xs, M, K, packed, absmax, N, ys, workspace,
+                                                    workspace_bytes, s);
+    return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+
+nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
+                      const float* absmax, int64_t N, int32_t block, uint16_t* y, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return nf4_linear_ex(x, NF4_DTYPE_BF16, M, K, packed, absmax, N, block, y, workspace, workspace_bytes, stream);
+}
+
+nf4_status nf4_linear_geglu_ex(const void* x, nf4_dtype dtype, int64_t M, int64_t K, const uint8_t* packed,
+                               const float* absmax, int64_t F, int32_t block, void* y, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (F >= (int64_t(1) << 30)) return NF4_ERR_SHAPE;   // 2F weight rows below 2^31
+    bool empty = false;
+    if (nf4_status st =
+            check_linear(x, dtype, M, K, packed, absmax, 2 * F, block, y, workspace, workspace_bytes, &empty);
+        st != NF4_OK || empty)
+        return st;
+    const nf4::DeviceInfo* dev = nullptr;
+    if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    uint16_t* ys = static_cast<uint16_t*>(y);
+    cudaError_t e = (M >= 128) ? nf4::launch_gemm_geglu(*dev, dtype, xs, M, K, packed, absmax, F, ys, s)
+                               : nf4::launch_skinny(*dev, dtype, xs, M, K, packed, absmax, 2 * F, ys, workspace,
+                                                    workspace_bytes, s, true);
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 
 nf4_status nf4_linear_geglu(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
                             const float* absmax, int64_t F, int32_t block, uint16_t* y, void* workspace,
                             size_t workspace_bytes, void* stream) {
-    if (block != NF4_BLOCK) return NF4_ERR_BLOCKSIZE;
-    if (M < 0 || F < 0 || K <= 0 || K % NF4_BLOCK != 0) return NF4_ERR_SHAPE;
-    // TMA coordinates are 32-bit: keep every extent (2F rows of weight) below 2^31.
-    if (M >= (int64_t(1) << 31) || F >= (int64_t(1) << 30) || K >= (int64_t(1) << 31)) return NF4_ERR_SHAPE;
-    if (M == 0 || F == 0) return NF4_OK;
-    if (!x || !packed || !absmax || !y) return NF4_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(y, 16) || !aligned(absmax, 4))
-        return NF4_ERR_ALIGN;
-    size_t need = 0;
-    nf4_linear_workspace_size(M, 2 * F, K, &need);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return NF4_ERR_WORKSPACE;
-        if (!aligned(workspace, 16)) return NF4_ERR_ALIGN;
-    }
-    const nf4::DeviceInfo* dev = nullptr;
-    if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = (M >= 128) ? nf4::launch_gemm_geglu(*dev, x, M, K, packed, absmax, F, y, s)
-                               : nf4::launch_skinny(*dev, x, M, K, packed, absmax, 2 * F, y, workspace,
-                                                    workspace_bytes, s, true);
-    return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+    return nf4_linear_geglu_ex(x, NF4_DTYPE_BF16, M, K, packed, absmax, F, block, y, workspace, workspace_bytes,
+                               stream);
 }
 
 nf4_status nf4_last_error(void* stream) {
@@ -189,6 +235,7 @@ const char* nf4_status_string(nf4_status status) {
         case NF4_ERR_DEVICE: return "NF4_ERR_DEVICE";
         case NF4_ERR_CUDA: return "NF4_ERR_CUDA";
         case NF4_ERR_TIMEOUT: return "NF4_ERR_TIMEOUT";
+        case NF4_ERR_DTYPE: return "NF4_ERR_DTYPE";
     }
     return "NF4_ERR_UNKNOWN";
 }

@@ -11,6 +11,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #ifndef NF4_WAIT_LIMIT_NS
@@ -123,27 +124,66 @@ __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
                  : "memory");
 }
 
-// ---------------------------------------------------------------- bf16 helpers
+// ---------------------------------------------------------------- element types
 
-// Two fp32 values -> one bf16x2 word (first in the low half), each rounded to
-// nearest even by the hardware conversion.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+// The compute dtype of weights, activations and outputs.  bf16 and fp16
+// travel as 16-bit patterns (two per 32-bit word, the element at the lower
+// address in the low half), fp32 as itself.
+enum : int { kBF16 = 0, kF16 = 1, kF32 = 2 };
+
+// Two fp32 values -> one word of two 16-bit values of type DT (first in the
+// low half), each rounded to nearest even by the hardware conversion.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    static_assert(DT == kBF16 || DT == kF16, "16-bit types");
+    uint32_t r;
+    if constexpr (DT == kBF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        r = *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        r = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return r;
 }
 
-// A LUT entry for packed byte b: bf16(C[b >> 4]) in the low half (the element
-// at the lower address) and bf16(C[b & 15]) in the high half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) { return pack2<kBF16>(lo, hi); }
+
+// A word of two 16-bit values of type DT -> the two fp32 values (exact).
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    static_assert(DT == kBF16 || DT == kF16, "16-bit types");
+    if constexpr (DT == kBF16) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        __half2 h = *reinterpret_cast<__half2*>(&w);
+        return __half22float2(h);
+    }
+}
+
+// One fp32 -> the 16-bit pattern of type DT, rounded to nearest even.
+template <int DT>
+__device__ __forceinline__ uint16_t round16(float v) {
+    static_assert(DT == kBF16 || DT == kF16, "16-bit types");
+    if constexpr (DT == kBF16)
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    else
+        return __half_as_ushort(__float2half_rn(v));
+}
+
+// A LUT entry for packed byte b: DT(C[b >> 4]) in the low half (the element
+// at the lower address) and DT(C[b & 15]) in the high half.
+template <int DT = kBF16>
 __device__ __forceinline__ uint32_t lut_entry(uint32_t b) {
-    return pack_bf16x2(c_code[b >> 4], c_code[b & 15]);
+    return pack2<DT>(c_code[b >> 4], c_code[b & 15]);
 }
 
-// Scale one LUT entry by the block absmax: each bf16 widened to fp32, one
-// fp32 multiply, one rounding back to bf16.
+// Scale one LUT entry by the block absmax: each value widened to fp32, one
+// fp32 multiply, one rounding back to DT.
+template <int DT = kBF16>
 __device__ __forceinline__ uint32_t scale_entry(uint32_t e, float am) {
-    float lo = __uint_as_float(e << 16);
-    float hi = __uint_as_float(e & 0xffff0000u);
-    return pack_bf16x2(lo * am, hi * am);
+    const float2 v = unpack2<DT>(e);
+    return pack2<DT>(v.x * am, v.y * am);
 }
 
 // ---------------------------------------------------------------- dependent launch
@@ -379,12 +419,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: bf16 A and B, fp32 D, both K-major,
-// no negation or sparsity; N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor for kind::f16: A and B both bf16 (DT = kBF16) or
+// both fp16 (DT = kF16) -- the two operands of one MMA always have the same
+// type -- fp32 D, both K-major, no negation or sparsity; N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+template <int DT = kBF16>
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N) {
+    static_assert(DT == kBF16 || DT == kF16, "kind::f16 operand types");
+    constexpr uint32_t ab = DT == kBF16 ? 1u : 0u;   // operand format: 0 fp16, 1 bf16
     return (1u << 4)            // D format: f32
-           | (1u << 7)          // A format: bf16
-           | (1u << 10)         // B format: bf16
+           | (ab << 7)          // A format
+           | (ab << 10)         // B format
            | (0u << 15)         // A K-major
            | (0u << 16)         // B K-major
            | (static_cast<uint32_t>(N >> 3) << 17)

@@ -38,6 +38,7 @@
 // records an error code, drains what it has in flight and returns.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include <cudaTypedefs.h>
 
@@ -108,19 +109,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// bf16x2 multiply with one round-to-nearest-even per half.
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+// Multiply of two words of two 16-bit values of type DT (bf16 or fp16),
+// one round-to-nearest-even per half.
+template <int DT>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
     uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    if constexpr (DT == kBF16)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
-// The 16 bf16 codebook values split into low bytes (l) and high bytes (h),
-// four codes per register: byte i of l[q] is the low byte of bf16(C[4q + i]).
+// The 16 codebook values of type DT split into low bytes (l) and high bytes
+// (h), four codes per register: byte i of l[q] is the low byte of DT(C[4q + i]).
 struct CodebookRegs {
     uint32_t l[4], h[4];
 };
 
+template <int DT>
 __device__ __forceinline__ CodebookRegs codebook_regs() {
     CodebookRegs cb;
 #pragma unroll
@@ -129,7 +136,7 @@ __device__ __forceinline__ CodebookRegs codebook_regs() {
         cb.h[q] = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(c_code[4 * q + i]));
+            const uint32_t bits = round16<DT>(c_code[4 * q + i]);
             cb.l[q] |= (bits & 0xffu) << (8 * i);
             cb.h[q] |= (bits >> 8) << (8 * i);
         }
@@ -149,30 +156,32 @@ __device__ __forceinline__ void lookup4(uint32_t s, const CodebookRegs& cb, uint
 }
 
 // One packed word (bytes in address order; byte j holds code 2j in its high
-// nibble) to four bf16x2 words, element 2i in the low half of word i, each
-// scaled by `am2`.  A bf16 x bf16 product is exact in fp32, so each value is
-// bf16_rne(float(bf16(C)) * absmax) -- the dequantizer's value -- whenever
-// absmax is a bf16 value, which every absmax nf4_quantize writes is (the max
-// of bf16 magnitudes).
+// nibble) to four words of two DT values, element 2i in the low half of word
+// i, each scaled by `am2`.  A product of two bf16 (or two fp16) values is
+// exact in fp32, so each value is DT_rne(float(DT(C)) * absmax) -- the
+// dequantizer's value -- whenever absmax is a DT value, which every absmax
+// nf4_quantize writes for a DT weight is (the max of DT magnitudes).
+template <int DT>
 __device__ __forceinline__ void expand8(uint32_t p, const CodebookRegs& cb, uint32_t am2, uint32_t* o) {
     uint32_t lo, hi;
     lookup4(p, cb, lo, hi);              // nibbles: code1, code0, code3, code2
-    o[0] = bf16x2_mul(prmt(lo, hi, 0x4051u), am2);
-    o[1] = bf16x2_mul(prmt(lo, hi, 0x6273u), am2);
+    o[0] = mul2<DT>(prmt(lo, hi, 0x4051u), am2);
+    o[1] = mul2<DT>(prmt(lo, hi, 0x6273u), am2);
     lookup4(p >> 16, cb, lo, hi);        // code5, code4, code7, code6
-    o[2] = bf16x2_mul(prmt(lo, hi, 0x4051u), am2);
-    o[3] = bf16x2_mul(prmt(lo, hi, 0x6273u), am2);
+    o[2] = mul2<DT>(prmt(lo, hi, 0x4051u), am2);
+    o[3] = mul2<DT>(prmt(lo, hi, 0x6273u), am2);
 }
 
 // expand8 through the shared-memory byte table instead of register permutes:
-// per packed byte one table load (the bf16 codebook values of its two codes,
-// element 2i in the low half) and one bf16x2 multiply.  `lut_lane` points at
+// per packed byte one table load (the DT codebook values of its two codes,
+// element 2i in the low half) and one paired multiply.  `lut_lane` points at
 // this lane's column of the replicated table (entry b at lut_lane[32 b]).
+template <int DT>
 __device__ __forceinline__ void expand8_lut(uint32_t p, const uint32_t* lut_lane, uint32_t am2, uint32_t* o) {
-    o[0] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4440u)], am2);
-    o[1] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4441u)], am2);
-    o[2] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4442u)], am2);
-    o[3] = bf16x2_mul(lut_lane[32u * prmt(p, 0u, 0x4443u)], am2);
+    o[0] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4440u)], am2);
+    o[1] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4441u)], am2);
+    o[2] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4442u)], am2);
+    o[3] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4443u)], am2);
 }
 
 // Whether a converter warp reports stage st as converted.  Always true in
@@ -367,11 +376,13 @@ struct TsArgs {
     uint32_t* err;
 };
 
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU>
+// DT: the compute dtype of X, Y and the converted weights (bf16 or fp16).
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
 __global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
     using C = TsCfg<NX, KS, RS, LUT, WS>;
+    static_assert(DT == kBF16 || DT == kF16, "kind::f16 operand types");
     static_assert(!(SPLIT && GEGLU), "a gate/up pair sums its split-K partials before the activation");
     // output columns per tile: 128 weight rows, or 64 gate/up row pairs
     constexpr int HW = GEGLU ? C::BW / 2 : C::BW;
@@ -405,7 +416,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
     if constexpr (LUT != 0) {
-        for (int e = threadIdx.x; e < 256 * 32; e += C::THREADS) lut[e] = lut_entry(static_cast<uint32_t>(e >> 5));
+        for (int e = threadIdx.x; e < 256 * 32; e += C::THREADS) lut[e] = lut_entry<DT>(static_cast<uint32_t>(e >> 5));
     }
     if (threadIdx.x == 0) {
         init_barriers(bar, C::CONV_WARPS, C::MI);
@@ -477,7 +488,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // weights and the activation tiles, one fence, the MMAs, one commit
         const int issuer = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, NX);
+            constexpr uint32_t idesc = idesc_f16kind_f32<DT>(128, NX);
             // the activation-tile descriptors differ only in the start-address
             // field (low 14 bits): one base plus a compile-time or per-stage offset
             const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_tile(0, 0)));
@@ -523,7 +534,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;             // weight row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        const CodebookRegs cb = codebook_regs();
+        const CodebookRegs cb = codebook_regs<DT>();
         bool ok = true;
         for (int ws = 0; ws < nws; ++ws) {
             const int p = ws % SP;
@@ -564,14 +575,14 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 if (st >= nst) break;
                 const int t = st % ST;
                 if (st * KS + h < nk) {                      // warp-uniform
-                    const uint32_t am2 = pack_bf16x2(am[w], am[w]);
+                    const uint32_t am2 = pack2<DT>(am[w], am[w]);
                     const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
                     const uint32_t* lut_lane = lut + lane;
                     auto expand = [&](uint32_t word, uint32_t* o) {
                         if (LUT == 1 || (LUT == 2 && part == 1))   // warp-uniform
-                            expand8_lut(word, lut_lane, am2, o);
+                            expand8_lut<DT>(word, lut_lane, am2, o);
                         else
-                            expand8(word, cb, am2, o);
+                            expand8<DT>(word, cb, am2, o);
                     };
                     if constexpr (RS == 1) {
                         uint32_t v[32];
@@ -661,8 +672,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                             const float g = gate ? mine : other;
                             const float up = gate ? other : mine;
                             if (m < args.M)
-                                args.y[static_cast<int64_t>(m) * args.N + n] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(g) * up));
+                                args.y[static_cast<int64_t>(m) * args.N + n] = round16<DT>(gelu_tanh(g) * up);
                         }
                     }
                 }
@@ -684,8 +694,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                             if constexpr (SPLIT) {
                                 args.ws[(static_cast<int64_t>(split) * args.M + m) * args.N + n] = __uint_as_float(v[i]);
                             } else {
-                                args.y[static_cast<int64_t>(m) * args.N + n] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i])));
+                                args.y[static_cast<int64_t>(m) * args.N + n] = round16<DT>(__uint_as_float(v[i]));
                             }
                         }
                     }
@@ -702,7 +711,8 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
 }
 
-// Sum the split-K partials in split order and round once to bf16.
+// Sum the split-K partials in split order and round once to DT.
+template <int DT>
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn,
                                      uint16_t* __restrict__ y) {
     pdl_wait();
@@ -711,13 +721,14 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float acc = ws[i];
         for (int s = 1; s < splits; ++s) acc += ws[static_cast<int64_t>(s) * mn + i];
-        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        y[i] = round16<DT>(acc);
     }
 }
 
 // Gate/up pair, M < 128: the split-K partials cover all 2F rows
 // ([splits, M, 2F]); sum the gate and the up partials in split order, then
-// write bf16(gelu(gate) * up), [M, F].
+// write DT(gelu(gate) * up), [M, F].
+template <int DT>
 __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t F,
                                            uint16_t* __restrict__ y) {
     pdl_wait();
@@ -732,7 +743,7 @@ __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int spl
             gs += g[s * mn2];
             us += g[s * mn2 + F];
         }
-        y[i] = __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(gs) * us));
+        y[i] = round16<DT>(gelu_tanh(gs) * us);
     }
 }
 
@@ -852,12 +863,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU>
+template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
     using C = TsCfg<NX, KS, RS, LUT, WS>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT, GEGLU>;
+    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT, GEGLU, DT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -869,32 +880,32 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS, int LUT, int WS, bool GEGLU>
+template <bool SPLIT, int KS, int RS, int LUT, int WS, bool GEGLU, int DT>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, false>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT, GEGLU>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -902,6 +913,7 @@ cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap&
 
 // N: rows of the weight.  pair: the weight is a gate/up pair ([2F, K], N = 2F)
 // and the GEGLU epilogue writes [M, F] (direct path only).
+template <int DT>
 cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const uint16_t* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, float* ws,
                         cudaStream_t s) {
@@ -912,32 +924,48 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const u
     const CUtensorMapSwizzle wsw = ks == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
                                  : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
                                            : CU_TENSOR_MAP_SWIZZLE_128B;
-    if (!make_map(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, p.nx, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    constexpr CUtensorMapDataType xdt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!make_map(&tm_x, x, xdt, 2, M, K, p.nx, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, pair ? kBW / 2 : kBW,
                   kPackedRow * ks, wsw))
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(pair ? N / 2 : N), static_cast<int>(K),
              p.kb_per_split, p.m_tiles, dev.err_word};
-    if (p.split) return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false>(dev, p, tm_x, tm_w, a, s);
-    return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true>(dev, p, tm_x, tm_w, a, s)
-                : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false>(dev, p, tm_x, tm_w, a, s);
+    if (p.split)
+        return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
+    return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true, DT>(dev, p, tm_x, tm_w, a, s)
+                : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false, DT>(dev, p, tm_x, tm_w, a, s);
+}
+
+// The element type at run time -> the kernels' compile-time DT.
+template <typename Fn>
+cudaError_t with_dt(int dtype, Fn&& fn) {
+    switch (dtype) {
+        case kBF16: return fn(std::integral_constant<int, kBF16>{});
+        case kF16: return fn(std::integral_constant<int, kF16>{});
+        default: return cudaErrorInvalidValue;   // no fp32 tensor-core path
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
-                        const float* absmax, int64_t N, uint16_t* y, cudaStream_t s) {
+cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, cudaStream_t s) {
     const Plan p = make_plan(M, N, K);
     if (p.split) return cudaErrorInvalidValue;
-    return launch_plan(dev, p, false, x, M, K, packed, absmax, N, y, nullptr, s);
+    return with_dt(dtype, [&](auto dt) {
+        return launch_plan<decltype(dt)::value>(dev, p, false, x, M, K, packed, absmax, N, y, nullptr, s);
+    });
 }
 
-cudaError_t launch_gemm_geglu(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
-                              const float* absmax, int64_t F, uint16_t* y, cudaStream_t s) {
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
+                              const uint8_t* packed, const float* absmax, int64_t F, uint16_t* y, cudaStream_t s) {
     // ceil(2F / 128) tiles of 128 weight rows = ceil(F / 64) tiles of 64 gate/up row pairs
     const Plan p = make_plan(M, 2 * F, K);
     if (p.split) return cudaErrorInvalidValue;
-    return launch_plan(dev, p, true, x, M, K, packed, absmax, 2 * F, y, nullptr, s);
+    return with_dt(dtype, [&](auto dt) {
+        return launch_plan<decltype(dt)::value>(dev, p, true, x, M, K, packed, absmax, 2 * F, y, nullptr, s);
+    });
 }
 
 size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K) {
@@ -947,24 +975,29 @@ size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K
 
 // N: rows of the weight; geglu: the weight is a gate/up pair (N = 2F) and
 // the reduction writes gelu(gate) * up, [M, F].
-cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
-                          const float* absmax, int64_t N, uint16_t* y, void* workspace, size_t ws_bytes,
-                          cudaStream_t s, bool geglu) {
+cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
+                          const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, void* workspace,
+                          size_t ws_bytes, cudaStream_t s, bool geglu) {
     const Plan p = make_plan(M, N, K);
     if (!p.split || ws_bytes < skinny_workspace_bytes(&dev, M, N, K) || (geglu && N % 2 != 0))
         return cudaErrorInvalidValue;
-    if (cudaError_t e = launch_plan(dev, p, false, x, M, K, packed, absmax, N, y, static_cast<float*>(workspace), s);
-        e != cudaSuccess)
-        return e;
-    const int64_t mn = geglu ? M * (N / 2) : M * N;   // outputs
-    const int threads = 256;
-    const int grid = static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
-    const float* wsf = static_cast<const float*>(workspace);
-    cudaError_t e = geglu ? launch_pdl(splitk_geglu_reduce_kernel, grid, threads, 0, s, wsf, p.splits, M, N / 2, y)
-                          : launch_pdl(splitk_reduce_kernel, grid, threads, 0, s, wsf, p.splits, mn, y);
-    if (e != cudaSuccess) return e;
-    count_launches(1);
-    return cudaGetLastError();
+    return with_dt(dtype, [&](auto dtc) {
+        constexpr int DT = decltype(dtc)::value;
+        if (cudaError_t e =
+                launch_plan<DT>(dev, p, false, x, M, K, packed, absmax, N, y, static_cast<float*>(workspace), s);
+            e != cudaSuccess)
+            return e;
+        const int64_t mn = geglu ? M * (N / 2) : M * N;   // outputs
+        const int threads = 256;
+        const int grid =
+            static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
+        const float* wsf = static_cast<const float*>(workspace);
+        cudaError_t e = geglu ? launch_pdl(splitk_geglu_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, M, N / 2, y)
+                              : launch_pdl(splitk_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, mn, y);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        return cudaGetLastError();
+    });
 }
 
 }  // namespace nf4

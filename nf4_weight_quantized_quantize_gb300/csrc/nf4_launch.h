@@ -47,14 +47,16 @@ void count_launches(int n);
 // nf4_capi.cu).  Returns 0 (NF4_OK) or an nf4_status code.
 int current_device_info(const DeviceInfo** out);
 
-cudaError_t launch_quantize(const DeviceInfo& dev, const uint16_t* w, int64_t numel, uint8_t* packed,
+// dtype: the element type of w / out (0 bf16, 1 fp16, 2 fp32, as nf4_dtype).
+cudaError_t launch_quantize(const DeviceInfo& dev, const void* w, int dtype, int64_t numel, uint8_t* packed,
                             float* absmax, cudaStream_t s);
 
 cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, const float* absmax,
-                              int64_t numel, uint16_t* out, cudaStream_t s);
+                              int64_t numel, int dtype, void* out, cudaStream_t s);
 
-// Fused NF4 GEMM, M >= 128 path (tcgen05 / TMEM).
-cudaError_t launch_gemm(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+// Fused NF4 GEMM, M >= 128 path (tcgen05 / TMEM).  dtype: the type of x, y
+// and the converted weights, bf16 (0) or fp16 (1).
+cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
                         cudaStream_t s);
 
@@ -63,14 +65,14 @@ size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64
 
 // Fused NF4 GEMM of a gate/up pair ([2F, K] weight, gate rows first) with the
 // GELU-gated product as epilogue, M >= 128: y [M, F] = gelu(X Wg^T) * (X Wu^T).
-cudaError_t launch_gemm_geglu(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
                               const uint8_t* packed, const float* absmax, int64_t F, uint16_t* y,
                               cudaStream_t s);
 
 // Skinny path: swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an
 // ordered reduction.  N is the weight's row count; with geglu the weight is a
 // gate/up pair (N = 2F) and the reduction writes gelu(gate) * up, [M, F].
-cudaError_t launch_skinny(const DeviceInfo& dev, const uint16_t* x, int64_t M, int64_t K,
+cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
                           const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
                           void* workspace, size_t ws_bytes, cudaStream_t s, bool geglu = false);
 

@@ -74,8 +74,8 @@ nf4_status nf4_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, const uin
     if (int st = nf4::current_device_info(&dev); st != NF4_OK) return static_cast<nf4_status>(st);
     void* scratch = nullptr;
     if (nf4_status st = scratch_address(dev->ordinal, &scratch); st != NF4_OK) return st;
-    cudaError_t e = nf4::launch_skinny(*dev, x, M, K, packed, absmax, N, y, scratch, kNoallocScratchBytes,
-                                       static_cast<cudaStream_t>(stream));
+    cudaError_t e = nf4::launch_skinny(*dev, NF4_DTYPE_BF16, x, M, K, packed, absmax, N, y, scratch,
+                                       kNoallocScratchBytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 

@@ -48,7 +48,7 @@ def test_library_links_no_torch_and_no_libcuda():
 def test_status_strings_and_version():
     for code, name in [(0, "NF4_OK"), (1, "NF4_ERR_NULL"), (2, "NF4_ERR_SHAPE"), (3, "NF4_ERR_ALIGN"),
                        (4, "NF4_ERR_BLOCKSIZE"), (5, "NF4_ERR_WORKSPACE"), (6, "NF4_ERR_DEVICE"),
-                       (7, "NF4_ERR_CUDA"), (8, "NF4_ERR_TIMEOUT")]:
+                       (7, "NF4_ERR_CUDA"), (8, "NF4_ERR_TIMEOUT"), (9, "NF4_ERR_DTYPE")]:
         assert nf4.nf4_status_string(code) == name
     assert nf4.nf4_status_string(99) == "NF4_ERR_UNKNOWN"
     assert nf4.nf4_version() >= 100
@@ -134,6 +134,26 @@ def test_linear_geglu_argument_errors():
     assert need > 0
     assert call(M=16, F=15360, K=3840) == nf4.NF4_ERR_WORKSPACE
     assert call(M=16, F=15360, K=3840, workspace=FAKE, workspace_bytes=need - 1) == nf4.NF4_ERR_WORKSPACE
+
+
+def test_dtype_argument_errors():
+    """The _ex entry points: a dtype outside nf4_dtype is refused on the host,
+    fp32 is refused by the tensor-core linears, element alignment follows the
+    dtype, and the plain entry points are their bf16 forms."""
+    BF16, F16, F32 = nf4.NF4_DTYPE_BF16, nf4.NF4_DTYPE_F16, nf4.NF4_DTYPE_F32
+    for bad in (-1, 3, 99):
+        assert nf4.nf4_quantize_ex(FAKE, bad, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_DTYPE
+        assert nf4.nf4_dequantize_ex(FAKE, FAKE, 128, 64, bad, FAKE) == nf4.NF4_ERR_DTYPE
+        assert nf4.nf4_linear_ex(FAKE, bad, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
+        assert nf4.nf4_linear_geglu_ex(FAKE, bad, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
+    assert nf4.nf4_linear_ex(FAKE, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
+    assert nf4.nf4_linear_geglu_ex(FAKE, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
+    assert nf4.nf4_quantize_ex(FAKE + 2, F32, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_quantize_ex(FAKE + 1, F16, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_dequantize_ex(FAKE, FAKE, 128, 64, F32, FAKE + 2) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_linear_ex(FAKE + 2, F16, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_quantize_ex(FAKE, BF16, 127, 64, FAKE, FAKE) == nf4.NF4_ERR_SHAPE
+    assert nf4.nf4_linear_ex(0, F16, 0, 128, 0, 0, 64, 64, 0, 0, 0) == nf4.NF4_OK
 
 
 def test_workspace_size_rules():

@@ -71,25 +71,27 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def make_weight(cfg: Linear, device="cpu", rows: slice | None = None) -> torch.Tensor:
-    """W [n, k] bf16 for `cfg` (the same tensor on every call with the same device)."""
+def make_weight(cfg: Linear, device="cpu", rows: slice | None = None, dtype=torch.bfloat16) -> torch.Tensor:
+    """W [n, k] for `cfg`, drawn in fp32 and cast to `dtype` (bf16 by default;
+    the same tensor on every call with the same device)."""
     g = _gen(cfg.w_seed, device)
     w = torch.randn(cfg.n, cfg.k, generator=g, device=device, dtype=torch.float32)
     w.mul_(cfg.w_std)
     if cfg.outlier_frac > 0:
         mask = torch.rand(cfg.n, cfg.k, generator=g, device=device) < cfg.outlier_frac
         w[mask] *= 20.0
-    w = w.to(torch.bfloat16)
+    w = w.to(dtype)
     return w if rows is None else w[rows].contiguous()
 
 
-def make_activation(cfg: Linear, device="cpu") -> torch.Tensor:
-    """X [m, k] bf16: `x_rows` (default m) rows are drawn and the first m kept, so a
-    skinny batch is a prefix of the full batch drawn with the same seed."""
+def make_activation(cfg: Linear, device="cpu", dtype=torch.bfloat16) -> torch.Tensor:
+    """X [m, k] of `dtype` (bf16 by default): `x_rows` (default m) rows are drawn
+    and the first m kept, so a skinny batch is a prefix of the full batch drawn
+    with the same seed."""
     g = _gen(cfg.x_seed, device)
     rows = max(cfg.m, cfg.x_rows)
     x = torch.randn(rows, cfg.k, generator=g, device=device, dtype=torch.float32)
-    x = x.to(torch.bfloat16)
+    x = x.to(dtype)
     return x[: cfg.m].contiguous()
 
 
@@ -103,3 +105,21 @@ def from_bits(a, device="cpu") -> torch.Tensor:
     import numpy as np
     t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
     return t.view(torch.bfloat16).to(device)
+
+
+def host(t: torch.Tensor):
+    """A tensor as the oracle takes it: numpy uint16 bit patterns for bf16 and
+    fp16, float32 values for fp32 (host copy)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view("uint16")
+
+
+def from_host(a, dtype, device="cpu") -> torch.Tensor:
+    """The inverse of host(): numpy data of the oracle's storage -> tensor of `dtype`."""
+    import numpy as np
+    a = np.ascontiguousarray(a)
+    if dtype == torch.float32:
+        return torch.from_numpy(a.astype(np.float32)).to(device)
+    return torch.from_numpy(a.view(np.int16)).view(dtype).to(device)
