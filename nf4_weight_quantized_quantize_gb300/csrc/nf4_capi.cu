@@ -91,7 +91,6 @@ nf4_status check_linear(const void* x, int dtype, int64_t M, int64_t K, const ui
     if (M < 0 || rows < 0 || K <= 0 || K % NF4_BLOCK != 0) return NF4_ERR_SHAPE;
     // TMA coordinates are 32-bit: keep every extent below 2^31.
     if (M >= (int64_t(1) << 31) || rows >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return NF4_ERR_SHAPE;
-    if (dtype == NF4_DTYPE_F32) return NF4_ERR_DTYPE;   // the tensor-core path takes bf16 and fp16
     if (M == 0 || rows == 0) {
         *empty = true;
         return NF4_OK;
@@ -167,10 +166,8 @@ nf4_status nf4_linear_ex(const void* x, nf4_dtype dtype, int64_t M, int64_t K, c
     const nf4::DeviceInfo* dev = nullptr;
     if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint16_t* xs = static_cast<const uint16_t*>(x);
-    uint16_t* ys = static_cast<uint16_t*>(y);
-    cudaError_t e = (M >= 128) ? nf4::launch_gemm(*dev, dtype, xs, M, K, packed, absmax, N, ys, s)
-                               : nf4::launch_skinny(*dev, dtype, xs, M, K, packed, absmax, N, ys, workspace,
+    cudaError_t e = (M >= 128) ? nf4::launch_gemm(*dev, dtype, x, M, K, packed, absmax, N, y, s)
+                               : nf4::launch_skinny(*dev, dtype, x, M, K, packed, absmax, N, y, workspace,
                                                     workspace_bytes, s);
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
@@ -193,10 +190,8 @@ nf4_status nf4_linear_geglu_ex(const void* x, nf4_dtype dtype, int64_t M, int64_
     const nf4::DeviceInfo* dev = nullptr;
     if (nf4_status st = current_device(&dev); st != NF4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint16_t* xs = static_cast<const uint16_t*>(x);
-    uint16_t* ys = static_cast<uint16_t*>(y);
-    cudaError_t e = (M >= 128) ? nf4::launch_gemm_geglu(*dev, dtype, xs, M, K, packed, absmax, F, ys, s)
-                               : nf4::launch_skinny(*dev, dtype, xs, M, K, packed, absmax, 2 * F, ys, workspace,
+    cudaError_t e = (M >= 128) ? nf4::launch_gemm_geglu(*dev, dtype, x, M, K, packed, absmax, F, y, s)
+                               : nf4::launch_skinny(*dev, dtype, x, M, K, packed, absmax, 2 * F, y, workspace,
                                                     workspace_bytes, s, true);
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }

@@ -360,6 +360,28 @@ __device__ __forceinline__ void mma_bf16_ts2(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// The same with kind::tf32: A (in TMEM) and B hold fp32 values of which the
+// tensor core reads the tf32 part (sign, exponent, 10 fraction bits); one MMA
+// covers K = 8 (32 bytes of a row, 8 TMEM columns of A).
+__device__ __forceinline__ void mma_tf32_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 bd, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// fp32 -> tf32, rounded to nearest (ties away from zero), as an fp32 bit
+// pattern whose low 13 bits are zero.
+__device__ __forceinline__ uint32_t to_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return r;
+}
+
 // Each thread stores 32 consecutive 32-bit columns of its own TMEM lane
 // (lane = 32 * (warp % 4) + lane id).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -432,6 +454,16 @@ __host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N) {
            | (ab << 10)         // B format
            | (0u << 15)         // A K-major
            | (0u << 16)         // B K-major
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::tf32: A and B tf32 (format 2), fp32 D,
+// both K-major; the other fields as for kind::f16.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)            // D format: f32
+           | (2u << 7)          // A format: tf32
+           | (2u << 10)         // B format: tf32
            | (static_cast<uint32_t>(N >> 3) << 17)
            | (static_cast<uint32_t>(M >> 4) << 24);
 }

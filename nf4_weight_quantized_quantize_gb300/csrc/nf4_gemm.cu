@@ -290,11 +290,18 @@ __device__ __forceinline__ void converters_sync(int threads) {
 
 // Compile-time layout of one kernel instance: NX activation rows per tile
 // (MMA N), stages of KS K-slices, RS converter threads per weight row and
-// K-slice (each expands 64 / RS of the row's values).
-template <int NX, int KS, int RS, int LUT, int WS>
+// K-slice (each expands 64 / RS of the row's values), EB bytes per element
+// of X and of the converted weights (2: bf16 / fp16, 4: fp32 read as tf32).
+template <int NX, int KS, int RS, int LUT, int WS, int EB = 2>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
-    static constexpr int XB = NX * kBK * 2;             // activation tile of one K-slice
+    static constexpr int XB = NX * kBK * EB;            // activation tile of one K-slice
+    // A K-slice row of X is kBK * EB bytes: EB / 2 sub-tiles of 128-byte rows
+    // (the 128-byte swizzle's span), XSUB bytes apart; one MMA covers 32 bytes
+    // of K, so a K-slice takes MMAS of them
+    static constexpr int XHALVES = EB / 2;
+    static constexpr int XSUB = NX * 128;
+    static constexpr int MMAS = kBK * EB / 32;
     // A weight-ring slot holds WS stages (WS * KS K-slices): the converter
     // warps wait on it once per WS stages.
     static constexpr int WK = KS * WS;                  // K-slices per weight slot
@@ -316,7 +323,8 @@ struct TsCfg {
     // accumulators, which keeps each accumulator's summation order fixed.
     static constexpr int MI = (NACC >= 2 && KS >= 2) ? 2 : 1;
     static constexpr int ACC_PER_MI = NACC / MI;
-    static constexpr int A_SLOT = 32 * KS;              // 64 bf16 per row per K-slice = 32 columns
+    static constexpr int A_COLS = kBK * EB / 4;         // TMEM columns of one K-slice row (32 or 64)
+    static constexpr int A_SLOT = A_COLS * KS;
     static constexpr int TMEM_SLOTS = (TMEM_COLS - A_COL0) / A_SLOT;
     static constexpr int SMEM_LIMIT = 232448;
     // LUT: a 256-entry bf16x2 byte table replicated once per lane (entry b of
@@ -338,7 +346,10 @@ struct TsCfg {
     // At least 120 KB, so no two CTAs share an SM: a second CTA there would
     // wait in tcgen05.alloc for the first one's 512 TMEM columns while
     // another SM idles.
-    static constexpr size_t USED = 1024 + OFF_BAR + Barriers::count(SX, ST, SP) * 8 + 16;
+    // after the barriers: the TMEM address, the abort flag and (fp32) the
+    // 16 fp32 codebook values
+    static constexpr int OFF_CODE = OFF_BAR + Barriers::count(SX, ST, SP) * 8 + 16;
+    static constexpr size_t USED = 1024 + OFF_CODE + 64;
     static constexpr size_t SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
     // warps: 0 activation producer, 1 MMA issuer, 2 .. 2 + CONV_WARPS - 1
     // converters (warp 2 + 4u + q: unit u, TMEM lane quarter q), then the
@@ -353,6 +364,7 @@ struct TsCfg {
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
     static_assert(WK == 1 || WK == 2 || WK == 4, "packed rows of 32, 64 or 128 bytes");
     static_assert(RS == 1 || RS == 2, "converter threads per row");
+    static_assert(EB == 2 || (EB == 4 && LUT == 0), "fp32 expands through the 16-entry code table");
     // The packed tile is loaded with the TMA swizzle whose span equals its
     // row (32 * WK bytes): the 16-byte chunk at byte offset o lands at chunk
     // (o / 16) XOR ((o / 128) mod 2 WK).  A converter warp reads one chunk
@@ -368,7 +380,7 @@ struct TsCfg {
 
 struct TsArgs {
     const float* absmax;  // [N, K/64] ([2N, K/64] for a gate/up pair)
-    uint16_t* y;          // [M, N] (direct, gate/up pair)
+    void* y;              // [M, N] of the compute dtype (direct, gate/up pair)
     float* ws;            // [splits, M, N] fp32 partials (split)
     int M, N, K;          // N: output columns (rows of one half of a gate/up pair)
     int kb_per_split;
@@ -376,13 +388,42 @@ struct TsArgs {
     uint32_t* err;
 };
 
-// DT: the compute dtype of X, Y and the converted weights (bf16 or fp16).
+// Element bytes of a compute dtype.
+template <int DT>
+constexpr int elem_bytes() {
+    return DT == kF32 ? 4 : 2;
+}
+
+// Store one output value in the compute dtype (16-bit types: one rounding
+// to nearest even).
+template <int DT>
+__device__ __forceinline__ void store_out(void* y, int64_t i, float v) {
+    if constexpr (DT == kF32)
+        static_cast<float*>(y)[i] = v;
+    else
+        static_cast<uint16_t*>(y)[i] = round16<DT>(v);
+}
+
+// fp32 weights: one packed word (bytes in address order, code 2j in the high
+// nibble of byte j) to eight values C[code] * absmax in fp32 -- the fp32
+// dequantizer's values -- rounded to tf32, the part the MMA reads.
+__device__ __forceinline__ void expand8_f32(uint32_t p, const float* code, float am, uint32_t* o) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = (p >> (8 * j)) & 0xffu;
+        o[2 * j] = to_tf32(code[b >> 4] * am);
+        o[2 * j + 1] = to_tf32(code[b & 15u] * am);
+    }
+}
+
+// DT: the compute dtype of X, Y and the converted weights: bf16 or fp16
+// (kind::f16) or fp32 (kind::tf32).
 template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
-__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS>::THREADS, 1)
+__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using C = TsCfg<NX, KS, RS, LUT, WS>;
-    static_assert(DT == kBF16 || DT == kF16, "kind::f16 operand types");
+    using C = TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>;
+    static_assert(DT == kBF16 || DT == kF16 || DT == kF32, "compute dtypes");
     static_assert(!(SPLIT && GEGLU), "a gate/up pair sums its split-K partials before the activation");
     // output columns per tile: 128 weight rows, or 64 gate/up row pairs
     constexpr int HW = GEGLU ? C::BW / 2 : C::BW;
@@ -417,6 +458,10 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
     if constexpr (LUT != 0) {
         for (int e = threadIdx.x; e < 256 * 32; e += C::THREADS) lut[e] = lut_entry<DT>(static_cast<uint32_t>(e >> 5));
+    }
+    float* code_f32 = reinterpret_cast<float*>(smem + C::OFF_CODE);
+    if constexpr (DT == kF32) {
+        if (threadIdx.x < 16) code_f32[threadIdx.x] = c_code[threadIdx.x];
     }
     if (threadIdx.x == 0) {
         init_barriers(bar, C::CONV_WARPS, C::MI);
@@ -454,8 +499,12 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 const int kb = kb0 + st * KS;
                 mbar_arrive_expect_tx(bar.xfull(s), C::X_SLOT);
 #pragma unroll
-                for (int h = 0; h < KS; ++h)
-                    tma_load_2d(smem_u32(x_tile(s, h)), &tm_x, bar.xfull(s), (kb + h) * kBK, m0);
+                for (int h = 0; h < KS; ++h) {
+#pragma unroll
+                    for (int x = 0; x < C::XHALVES; ++x)   // 128-byte column blocks of the K-slice
+                        tma_load_2d(smem_u32(x_tile(s, h) + x * C::XSUB), &tm_x, bar.xfull(s),
+                                    (kb + h) * kBK + x * (kBK / C::XHALVES), m0);
+                }
                 ++issued;
             }
             if (*abort_flag) drain_ring(bar.xfull(0), SX, issued, args.err);
@@ -488,7 +537,12 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         // weights and the activation tiles, one fence, the MMAs, one commit
         const int issuer = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16kind_f32<DT>(128, NX);
+            constexpr uint32_t idesc = [] {
+                if constexpr (DT == kF32)
+                    return idesc_tf32_f32(128, NX);
+                else
+                    return idesc_f16kind_f32<DT>(128, NX);
+            }();
             // the activation-tile descriptors differ only in the start-address
             // field (low 14 bits): one base plus a compile-time or per-stage offset
             const uint64_t xdesc0 = smem_desc_sw128(smem_u32(x_tile(0, 0)));
@@ -511,10 +565,18 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 for (int h = 0; h < KS; ++h) {
                     if (h % C::MI == issuer && h < kbs) {
 #pragma unroll
-                        for (int j = 0; j < kBK / 16; ++j)
-                            mma_bf16_ts2(acc0 + (j % C::ACC_PER_MI) * C::ACC_STRIDE, a_col + 32 * h + 8 * j,
-                                         x_lo + static_cast<uint32_t>((h * C::XB + 32 * j) >> 4), x_hi, idesc,
-                                         (h >= C::MI || j >= C::ACC_PER_MI) ? 1u : first);
+                        for (int j = 0; j < C::MMAS; ++j) {
+                            // 32 bytes of K: 8 TMEM columns of A; B at byte 32 (j % 4)
+                            // of the rows of sub-tile j / 4
+                            const uint32_t d = acc0 + (j % C::ACC_PER_MI) * C::ACC_STRIDE;
+                            const uint32_t a = a_col + C::A_COLS * h + 8 * j;
+                            const uint32_t b = x_lo + static_cast<uint32_t>((h * C::XB + (j / 4) * C::XSUB + 32 * (j % 4)) >> 4);
+                            const uint32_t acc = (h >= C::MI || j >= C::ACC_PER_MI) ? 1u : first;
+                            if constexpr (DT == kF32)
+                                mma_tf32_ts2(d, a, b, x_hi, idesc, acc);
+                            else
+                                mma_bf16_ts2(d, a, b, x_hi, idesc, acc);
+                        }
                     }
                 }
                 mma_commit(bar.done(t));
@@ -534,7 +596,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;             // weight row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        const CodebookRegs cb = codebook_regs<DT>();
+        const CodebookRegs cb = codebook_regs<DT == kF32 ? kBF16 : DT>();
         bool ok = true;
         for (int ws = 0; ws < nws; ++ws) {
             const int p = ws % SP;
@@ -574,15 +636,33 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 const int st = WS * ws + w;
                 if (st >= nst) break;
                 const int t = st % ST;
-                if (st * KS + h < nk) {                      // warp-uniform
-                    const uint32_t am2 = pack2<DT>(am[w], am[w]);
-                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + 32 * h;
+                if (DT == kF32 && st * KS + h < nk) {        // warp-uniform
+                    // 64 fp32 values per row and K-slice: 64 TMEM columns
+                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + C::A_COLS * h;
+                    uint32_t v[32];
+                    expand8_f32(q0[w].x, code_f32, am[w], v + 0);
+                    expand8_f32(q0[w].y, code_f32, am[w], v + 8);
+                    expand8_f32(q0[w].z, code_f32, am[w], v + 16);
+                    expand8_f32(q0[w].w, code_f32, am[w], v + 24);
+                    tmem_st32(col + 32 * (RS == 1 ? 0 : part), v);
+                    if constexpr (RS == 1) {
+                        expand8_f32(q1[w].x, code_f32, am[w], v + 0);
+                        expand8_f32(q1[w].y, code_f32, am[w], v + 8);
+                        expand8_f32(q1[w].z, code_f32, am[w], v + 16);
+                        expand8_f32(q1[w].w, code_f32, am[w], v + 24);
+                        tmem_st32(col + 32, v);
+                    }
+                    tmem_st_wait();
+                } else if (DT != kF32 && st * KS + h < nk) {   // warp-uniform
+                    const uint32_t am2 = pack2<DT == kF32 ? kBF16 : DT>(am[w], am[w]);
+                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + C::A_COLS * h;
                     const uint32_t* lut_lane = lut + lane;
+                    constexpr int D16 = DT == kF32 ? kBF16 : DT;
                     auto expand = [&](uint32_t word, uint32_t* o) {
                         if (LUT == 1 || (LUT == 2 && part == 1))   // warp-uniform
-                            expand8_lut<DT>(word, lut_lane, am2, o);
+                            expand8_lut<D16>(word, lut_lane, am2, o);
                         else
-                            expand8<DT>(word, cb, am2, o);
+                            expand8<D16>(word, cb, am2, o);
                     };
                     if constexpr (RS == 1) {
                         uint32_t v[32];
@@ -671,8 +751,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                             const float other = xbuf[(c0 + i) * HW + rr];
                             const float g = gate ? mine : other;
                             const float up = gate ? other : mine;
-                            if (m < args.M)
-                                args.y[static_cast<int64_t>(m) * args.N + n] = round16<DT>(gelu_tanh(g) * up);
+                            if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, gelu_tanh(g) * up);
                         }
                     }
                 }
@@ -694,7 +773,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                             if constexpr (SPLIT) {
                                 args.ws[(static_cast<int64_t>(split) * args.M + m) * args.N + n] = __uint_as_float(v[i]);
                             } else {
-                                args.y[static_cast<int64_t>(m) * args.N + n] = round16<DT>(__uint_as_float(v[i]));
+                                store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, __uint_as_float(v[i]));
                             }
                         }
                     }
@@ -711,17 +790,16 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
 }
 
-// Sum the split-K partials in split order and round once to DT.
+// Sum the split-K partials in split order and store once in DT.
 template <int DT>
-__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn,
-                                     uint16_t* __restrict__ y) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn, void* __restrict__ y) {
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < mn;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float acc = ws[i];
         for (int s = 1; s < splits; ++s) acc += ws[static_cast<int64_t>(s) * mn + i];
-        y[i] = round16<DT>(acc);
+        store_out<DT>(y, i, acc);
     }
 }
 
@@ -730,7 +808,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
 // write DT(gelu(gate) * up), [M, F].
 template <int DT>
 __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t F,
-                                           uint16_t* __restrict__ y) {
+                                           void* __restrict__ y) {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t mn2 = M * 2 * F;
@@ -743,7 +821,7 @@ __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int spl
             gs += g[s * mn2];
             us += g[s * mn2 + F];
         }
-        y[i] = round16<DT>(gelu_tanh(gs) * us);
+        store_out<DT>(y, i, gelu_tanh(gs) * us);
     }
 }
 
@@ -779,6 +857,11 @@ constexpr int kLutSplit = NF4_LUT_SPLIT;
 #endif
 constexpr int kWsDirect = NF4_WS_DIRECT;     // stages per weight-ring slot, M >= 128
 constexpr int kWsSplit = 1;                  // stages per weight-ring slot, M < 128
+// fp32 (tf32 MMA): activation tiles twice as large, so fewer K-slices per
+// stage; the 16-entry fp32 code table instead of the byte tables.
+constexpr int kKsDirectF32 = 1, kRsDirectF32 = 2;
+constexpr int kKsSplitF32 = 2, kRsSplitF32 = 1;
+static_assert(kKsSplit % kKsSplitF32 == 0, "split-K ranges are whole stages at every dtype");
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -866,7 +949,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
 template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    using C = TsCfg<NX, KS, RS, LUT, WS>;
+    using C = TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
     auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT, GEGLU, DT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
@@ -914,27 +997,40 @@ cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap&
 // N: rows of the weight.  pair: the weight is a gate/up pair ([2F, K], N = 2F)
 // and the GEGLU epilogue writes [M, F] (direct path only).
 template <int DT>
-cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const uint16_t* x, int64_t M, int64_t K,
-                        const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, float* ws,
+cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const void* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t N, void* y, float* ws,
                         cudaStream_t s) {
     if (pair && (p.split || N % 2 != 0)) return cudaErrorInvalidValue;
     CUtensorMap tm_x, tm_w;
-    const int ks = p.split ? kKsSplit * kWsSplit : kKsDirect * kWsDirect;   // K-slices per weight slot
+    constexpr bool F32 = DT == kF32;
+    const int ks = p.split ? (F32 ? kKsSplitF32 : kKsSplit) * kWsSplit
+                           : (F32 ? kKsDirectF32 : kKsDirect) * kWsDirect;   // K-slices per weight slot
     // the packed box row is 32 * ks bytes; its swizzle span matches (TsCfg::packed_offset)
     const CUtensorMapSwizzle wsw = ks == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
                                  : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
                                            : CU_TENSOR_MAP_SWIZZLE_128B;
-    constexpr CUtensorMapDataType xdt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!make_map(&tm_x, x, xdt, 2, M, K, p.nx, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    constexpr CUtensorMapDataType xdt = DT == kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : DT == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    constexpr int eb = elem_bytes<DT>();
+    // one box = 128 bytes of a row (the swizzle span): 64 16-bit or 32 fp32 values
+    if (!make_map(&tm_x, x, xdt, eb, M, K, p.nx, 128 / eb, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, pair ? kBW / 2 : kBW,
                   kPackedRow * ks, wsw))
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(pair ? N / 2 : N), static_cast<int>(K),
              p.kb_per_split, p.m_tiles, dev.err_word};
-    if (p.split)
-        return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
-    return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true, DT>(dev, p, tm_x, tm_w, a, s)
-                : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false, DT>(dev, p, tm_x, tm_w, a, s);
+    if constexpr (F32) {
+        if (p.split)
+            return dispatch_nx<true, kKsSplitF32, kRsSplitF32, 0, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
+        return pair ? dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, 1, true, DT>(dev, p, tm_x, tm_w, a, s)
+                    : dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, 1, false, DT>(dev, p, tm_x, tm_w, a, s);
+    } else {
+        if (p.split)
+            return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
+        return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true, DT>(dev, p, tm_x, tm_w, a, s)
+                    : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false, DT>(dev, p, tm_x, tm_w, a, s);
+    }
 }
 
 // The element type at run time -> the kernels' compile-time DT.
@@ -943,14 +1039,15 @@ cudaError_t with_dt(int dtype, Fn&& fn) {
     switch (dtype) {
         case kBF16: return fn(std::integral_constant<int, kBF16>{});
         case kF16: return fn(std::integral_constant<int, kF16>{});
-        default: return cudaErrorInvalidValue;   // no fp32 tensor-core path
+        case kF32: return fn(std::integral_constant<int, kF32>{});
+        default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                        const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, cudaStream_t s) {
+cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
     const Plan p = make_plan(M, N, K);
     if (p.split) return cudaErrorInvalidValue;
     return with_dt(dtype, [&](auto dt) {
@@ -958,8 +1055,8 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const uint16_t* x, int
     });
 }
 
-cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                              const uint8_t* packed, const float* absmax, int64_t F, uint16_t* y, cudaStream_t s) {
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                              const uint8_t* packed, const float* absmax, int64_t F, void* y, cudaStream_t s) {
     // ceil(2F / 128) tiles of 128 weight rows = ceil(F / 64) tiles of 64 gate/up row pairs
     const Plan p = make_plan(M, 2 * F, K);
     if (p.split) return cudaErrorInvalidValue;
@@ -975,8 +1072,8 @@ size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K
 
 // N: rows of the weight; geglu: the weight is a gate/up pair (N = 2F) and
 // the reduction writes gelu(gate) * up, [M, F].
-cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                          const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y, void* workspace,
+cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                          const uint8_t* packed, const float* absmax, int64_t N, void* y, void* workspace,
                           size_t ws_bytes, cudaStream_t s, bool geglu) {
     const Plan p = make_plan(M, N, K);
     if (!p.split || ws_bytes < skinny_workspace_bytes(&dev, M, N, K) || (geglu && N % 2 != 0))

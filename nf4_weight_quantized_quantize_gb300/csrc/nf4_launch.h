@@ -55,9 +55,9 @@ cudaError_t launch_dequantize(const DeviceInfo& dev, const uint8_t* packed, cons
                               int64_t numel, int dtype, void* out, cudaStream_t s);
 
 // Fused NF4 GEMM, M >= 128 path (tcgen05 / TMEM).  dtype: the type of x, y
-// and the converted weights, bf16 (0) or fp16 (1).
-cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                        const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
+// and the converted weights, bf16 (0), fp16 (1) or fp32 (2, tf32 MMA).
+cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t N, void* y,
                         cudaStream_t s);
 
 // Workspace bytes the skinny (M < 128) path needs for this shape.
@@ -65,15 +65,15 @@ size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64
 
 // Fused NF4 GEMM of a gate/up pair ([2F, K] weight, gate rows first) with the
 // GELU-gated product as epilogue, M >= 128: y [M, F] = gelu(X Wg^T) * (X Wu^T).
-cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                              const uint8_t* packed, const float* absmax, int64_t F, uint16_t* y,
+cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                              const uint8_t* packed, const float* absmax, int64_t F, void* y,
                               cudaStream_t s);
 
 // Skinny path: swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an
 // ordered reduction.  N is the weight's row count; with geglu the weight is a
 // gate/up pair (N = 2F) and the reduction writes gelu(gate) * up, [M, F].
-cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const uint16_t* x, int64_t M, int64_t K,
-                          const uint8_t* packed, const float* absmax, int64_t N, uint16_t* y,
+cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                          const uint8_t* packed, const float* absmax, int64_t N, void* y,
                           void* workspace, size_t ws_bytes, cudaStream_t s, bool geglu = false);
 
 }  // namespace nf4

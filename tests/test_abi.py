@@ -137,17 +137,17 @@ def test_linear_geglu_argument_errors():
 
 
 def test_dtype_argument_errors():
-    """The _ex entry points: a dtype outside nf4_dtype is refused on the host,
-    fp32 is refused by the tensor-core linears, element alignment follows the
-    dtype, and the plain entry points are their bf16 forms."""
+    """The _ex entry points: a dtype outside nf4_dtype is refused on the host
+    and element alignment follows the dtype.  (No call here passes
+    validation with its placeholder pointers.)"""
     BF16, F16, F32 = nf4.NF4_DTYPE_BF16, nf4.NF4_DTYPE_F16, nf4.NF4_DTYPE_F32
     for bad in (-1, 3, 99):
         assert nf4.nf4_quantize_ex(FAKE, bad, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_DTYPE
         assert nf4.nf4_dequantize_ex(FAKE, FAKE, 128, 64, bad, FAKE) == nf4.NF4_ERR_DTYPE
         assert nf4.nf4_linear_ex(FAKE, bad, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
         assert nf4.nf4_linear_geglu_ex(FAKE, bad, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
-    assert nf4.nf4_linear_ex(FAKE, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
-    assert nf4.nf4_linear_geglu_ex(FAKE, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_DTYPE
+    assert nf4.nf4_linear_ex(FAKE + 4, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE, 0, 0) == nf4.NF4_ERR_ALIGN
+    assert nf4.nf4_linear_geglu_ex(FAKE, F32, 256, 128, FAKE, FAKE, 64, 64, FAKE + 8, 0, 0) == nf4.NF4_ERR_ALIGN
     assert nf4.nf4_quantize_ex(FAKE + 2, F32, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_ALIGN
     assert nf4.nf4_quantize_ex(FAKE + 1, F16, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_ALIGN
     assert nf4.nf4_dequantize_ex(FAKE, FAKE, 128, 64, F32, FAKE + 2) == nf4.NF4_ERR_ALIGN

@@ -7,7 +7,9 @@ end in a partial tile or block, unaligned pointers (the element-wise
 kernels), and blocks whose absmax is subnormal.  The fp16 linear and the
 fp16 gate/up pair are compared with the oracle's fp64 result of the same
 fp16 inputs within the row-normalised tolerance of the bf16 linear, plus a
-per-element bound of fp16 output rounding and fp32 summation error.
+per-element bound of fp16 output rounding and fp32 summation error; the fp32
+ones (tf32 tensor-core products) the same way with the tf32 operand error
+in the bound.
 """
 import numpy as np
 import pytest
@@ -176,13 +178,69 @@ def test_f16_matches_bf16_path_on_shared_values():
     assert ((ys[0] - ys[1]).abs() / ref).max().item() < 1e-2
 
 
-def test_fp32_linear_is_refused():
-    x = torch.zeros(256, 128, dtype=torch.float32, device=DEV)
-    p = torch.zeros(64 * 64, dtype=torch.uint8, device=DEV)
-    a = torch.zeros(128, dtype=torch.float32, device=DEV)
-    with pytest.raises(nf4.NF4Error) as e:
-        nf4.linear(x, p, a, 64)
-    assert e.value.status == nf4.NF4_ERR_DTYPE
+# ---------------------------------------------------------------- fp32 linear (tf32 MMA)
+
+
+def linear_check(dtype, x_cpu, w_cpu, fn, n_cols, oracle_fn, rows=None):
+    """Run the GEMM `fn` at `dtype` and compare (the sampled `rows` of) its
+    result with the oracle's fp64 result of the same rows; returns the
+    compared arrays."""
+    p, a = oracle.quantize(workloads.host(w_cpu), dtype=dtype)
+    y = fn(x_cpu.to(DEV), torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV))
+    torch.cuda.synchronize()
+    assert y.dtype == TORCH[dtype] and y.shape == (x_cpu.shape[0], n_cols)
+    yg = y.float().cpu().numpy().astype(np.float64)
+    xb = workloads.host(x_cpu)
+    if rows is not None:
+        yg, xb = yg[rows], xb[rows]
+    yref = oracle_fn(xb, p, a)
+    nrm = np.linalg.norm(yref, axis=1, keepdims=True)
+    err = float(np.max(np.abs(yg - yref) / np.maximum(nrm, 1e-300)))
+    assert err <= TOL, f"row-normalised error {err}"
+    return yg, yref, xb, p, a
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 3840), (16, 3840, 15360), (257, 300, 128), (130, 640, 1536),
+                                   (33, 1000, 64 * 50), (512, 256, 64)])
+def test_linear_f32(M, N, K):
+    """fp32 compute dtype: the tensor cores read tf32 (X's 10-bit fraction,
+    the weight rounded to tf32), accumulate in fp32 and write fp32.  Per
+    element each product is within 2^-9 relative of the exact one, so
+    |Y - Yref| <= (2^-9 + K 2^-23) sum_k |x_k| |w_k|."""
+    seed = 7 * M + N + K
+    w = rand_w(N * K, 0.02, seed, "f32").reshape(N, K)
+    x = rand_w(M * K, 1.0, seed + 1, "f32").reshape(M, K)
+    rows = None if M * N <= 1 << 20 else np.sort(np.random.default_rng(M).choice(M, 32, replace=False))
+    ys, yref, xs, p, a = linear_check("f32", x, w, lambda xd, pd, ad: nf4.linear(xd, pd, ad, N), N,
+                                      lambda xb, p, a: oracle.linear(xb, p, a, N, dtype="f32"), rows)
+    wd = oracle.dequantize(p, a, N * K, dtype="f32").astype(np.float64).reshape(N, K)
+    mag = np.abs(xs.astype(np.float64)) @ np.abs(wd).T
+    bound = (2.0 ** -9 + K * 2.0 ** -23) * mag + 1e-30
+    assert not (np.abs(ys - yref) > bound).any()
+
+
+@pytest.mark.parametrize("M", [300, 16])
+def test_linear_geglu_f32(M):
+    F, K = 640, 1024
+    w = rand_w(2 * F * K, 0.05, 190 + M, "f32").reshape(2 * F, K)
+    x = rand_w(M * K, 1.0, 191 + M, "f32").reshape(M, K)
+    linear_check("f32", x, w, lambda xd, pd, ad: nf4.linear_geglu(xd, pd, ad, F), F,
+                 lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f32"))
+
+
+def test_f32_close_to_bf16_on_shared_values():
+    """Weights and activations exactly representable in bf16: the fp32 (tf32)
+    and bf16 GEMMs agree to within the bf16 roundings."""
+    rs = np.random.default_rng(4)
+    N, K, M = 384, 768, 300
+    w = torch.from_numpy((rs.integers(-64, 64, (N, K)) * 2.0 ** -8).astype(np.float32))
+    x = torch.from_numpy((rs.integers(-8, 8, (M, K)) * 2.0 ** -2).astype(np.float32))
+    ys = []
+    for dt in (torch.bfloat16, torch.float32):
+        p, a = nf4.quantize(w.to(dt).to(DEV))
+        ys.append(nf4.linear(x.to(dt).to(DEV), p, a, N).float())
+    ref = ys[1].abs().amax(dim=1, keepdim=True)
+    assert ((ys[0] - ys[1]).abs() / ref).max().item() < 1e-2
 
 
 def test_no_error_recorded():
