@@ -462,6 +462,8 @@ def run_ours(args):
     }
     if not args.no_geglu:
         line["geglu"] = geglu_block(dev)
+    if not args.no_dtypes:
+        line["dtypes"] = dtypes_block(dev)
     if not args.no_stack:
         line["stack"] = stack_block(dev)
     if not args.no_cpu_baseline:
@@ -524,6 +526,65 @@ def geglu_block(dev, reps: int = 20):
         "m16": {"fused_ms": t_fused_s, "unfused_linear_ms": t_plain_s},
         "timing": f"mean of {reps} calls, CUDA events, 512 MiB L2 flush before each",
     }
+
+
+def dtypes_block(dev, reps: int = 20):
+    """The three compute dtypes on the q_proj workload (W [4096, 3840], X
+    [2048, 3840]): nf4_quantize_ex, nf4_dequantize_ex and nf4_linear_ex, mean
+    of `reps` calls with the L2 flushed before each.  Bytes per weight:
+    quantize e + 0.5625, dequantize 0.5625 + e (e = 2 for bf16 / fp16, 4 for
+    fp32).  The fp32 linear runs on the tf32 tensor cores; its peak is the
+    measured bf16 peak times the nominal dense tf32 : bf16 ratio 1.1 : 2.25."""
+    import torch
+    import nf4_weight_quantized_quantize_gb300 as nf4
+
+    cfg = CFG
+    stream = torch.cuda.current_stream(dev)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    pk, pk_kind = peaks()
+    out = {"workload": cfg.name, "timing": f"mean of {reps} calls, CUDA events, 512 MiB L2 flush before each"}
+
+    def timed(fn):
+        fn()
+        ev = [(mk(), mk()) for _ in range(reps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    for name, dt in (("bf16", torch.bfloat16), ("f16", torch.float16), ("f32", torch.float32)):
+        eb = torch.tensor([], dtype=dt).element_size()
+        w = workloads.make_weight(cfg, device=dev, dtype=dt)
+        x = workloads.make_activation(cfg, device=dev, dtype=dt)
+        numel = w.numel()
+        p = torch.empty(numel // 2, dtype=torch.uint8, device=dev)
+        a = torch.empty(numel // 64, dtype=torch.float32, device=dev)
+        wd = torch.empty(numel, dtype=dt, device=dev)
+        y = torch.empty(cfg.m, cfg.n, dtype=dt, device=dev)
+        t_q = timed(lambda: nf4.quantize(w, out=(p, a)))
+        t_d = timed(lambda: nf4.dequantize(p, a, numel, out=wd))
+        t_l = timed(lambda: nf4.linear(x, p, a, cfg.n, out=y))
+        tf = 2 * cfg.m * cfg.n * cfg.k / (t_l * 1e-3) / 1e12
+        peak = pk["bf16_tflops"] * (1.1 / 2.25 if name == "f32" else 1.0)
+        out[name] = {
+            "quantize": {"ms": t_q, "GB/s": numel * (eb + 0.5625) / (t_q * 1e-3) / 1e9},
+            "dequantize": {"ms": t_d, "GB/s": numel * (0.5625 + eb) / (t_d * 1e-3) / 1e9},
+            "linear_m2048": {"ms": t_l, "TFLOP/s": tf, "frac_peak": tf / peak,
+                             "peak": ("tf32 = bf16 x 1.1/2.25 (nominal ratio), " if name == "f32" else "bf16, ")
+                             + f"of {pk_kind}"},
+        }
+        for k in ("quantize", "dequantize"):
+            out[name][k]["frac_hbm"] = out[name][k]["GB/s"] / pk["hbm_gbs"]
+        del w, x, p, a, wd, y
+    if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
+        raise RuntimeError("a kernel reported a timeout in the dtype measurement")
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def stack_block(dev, passes: int = 2):
@@ -625,6 +686,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="omit the CPU oracle timing")
     ap.add_argument("--no-stack", action="store_true", help="omit the 48-layer stack measurement")
     ap.add_argument("--no-geglu", action="store_true", help="omit the fused gate/up measurement")
+    ap.add_argument("--no-dtypes", action="store_true", help="omit the fp16 / fp32 measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
