@@ -110,7 +110,7 @@ __device__ __forceinline__ uint32_t code_from_estimate(float q, float hm, const 
 }
 
 // Below the smallest normal fp32 the reciprocal of an absmax can overflow:
-// such blocks (bf16 or fp32 subnormals only) take the exact path.
+// words of such blocks (bf16 or fp32 subnormals only) take the exact path.
 constexpr float kMinNormal = 0x1p-126f;
 
 // The packed byte of two values (w0 in the high nibble): the quotients and
@@ -143,10 +143,11 @@ template <int DT>
 __device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, const float* s_thr) {
     if (am_bits == 0u) return 0x77777777u;
     const float am = am_of<DT>(am_bits);
-    if (am < kMinNormal) return quantize8<DT>(v, am_bits, s_thr);
     const float rcp = __frcp_rn(am);
     const uint64_t rcp2 = pack_f32x2(rcp, rcp);
-    bool exact_needed = false;
+    // a subnormal absmax: the reciprocal may be infinite, the estimates then
+    // unspecified (but in range) -- take the exact path for the whole word
+    bool exact_needed = am < kMinNormal;
     const uint32_t out = code_pair16<DT>(v.x, rcp2, s_thr, exact_needed) |
                          (code_pair16<DT>(v.y, rcp2, s_thr, exact_needed) << 8) |
                          (code_pair16<DT>(v.z, rcp2, s_thr, exact_needed) << 16) |
@@ -158,7 +159,7 @@ __device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, co
 // bytes (the first in the low byte), fast path with the exact fallback.
 __device__ __forceinline__ uint32_t quantize4_f32_fast(uint4 v, float am, const float* s_thr) {
     if (am == 0.0f) return 0x7777u;
-    if (am < kMinNormal)
+    if (am < kMinNormal)   // as in quantize8_fast; an early exit keeps this kernel within 32 registers
         return code_byte_exact(__uint_as_float(v.x), __uint_as_float(v.y), am, s_thr) |
                (code_byte_exact(__uint_as_float(v.z), __uint_as_float(v.w), am, s_thr) << 8);
     const float rcp = __frcp_rn(am);
