@@ -89,7 +89,8 @@ typedef enum nf4_dtype {
 
 /*
  * nf4_quantize -- blockwise absmax NF4 quantization of one bf16 tensor.
- * Page: "Gemma3 NF4 on GPU" (#39), Summary: projection weights "pack to NF4".
+ * Page: "Gemma3 NF4 on GPU" (#39), Summary: the projection weights are packed
+ * to NF4.
  *
  *   w       [numel] bf16 bits, any layout the caller flattens row-major
  *   numel   number of elements; even, >= 0 (0 enqueues nothing)

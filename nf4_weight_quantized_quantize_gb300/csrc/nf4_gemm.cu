@@ -1,6 +1,7 @@
 // nf4_gemm.cu -- fused NF4 weight-only GEMM on the 5th-generation tensor
-// cores: Y[M, N] = X[M, K] . deq(W)[N, K]^T, bf16 in, fp32 accumulate in TMEM,
-// bf16 out.
+// cores: Y[M, N] = X[M, K] . deq(W)[N, K]^T with X, Y and the dequantized
+// weight in the compute dtype -- bf16 or fp16 (tcgen05 kind::f16) or fp32
+// (kind::tf32) -- and fp32 accumulation in TMEM.
 //
 // This is the forward of the NF4 linear module of the diffuseR page "Gemma3
 // NF4 on GPU" (#39, Summary: ltx23_nf4_linear, dequantize then a dense matmul
@@ -8,14 +9,14 @@
 // calling a dense GEMM, each CTA expands its packed weight tile in registers
 // and writes it straight into tensor memory, where the MMA reads it, so the
 // weight crosses HBM at 0.5625 bytes per element and never touches shared
-// memory in bf16 form.
+// memory in expanded form.
 //
 // One kernel template, three uses:
 //   direct (M >= 128): CTA tile = 128 weight rows x NX activation rows
-//       (NX <= 256), the whole K range, bf16 Y written by the epilogue.
+//       (NX <= 256), the whole K range, Y written by the epilogue.
 //   split (M < 128):  NX = M rounded up to 16, K split over CTAs so every SM
 //       streams weights; fp32 partials to a workspace, then an ordered
-//       reduction kernel writes bf16 Y.
+//       reduction kernel writes Y.
 //   gate/up pair (GEGLU, M >= 128): the weight is the Gemma3 MLP's gate and
 //       up projections stacked into one [2F, K] tensor; a tile's 128 rows are
 //       64 gate rows and the 64 up rows of the same outputs, and the epilogue
@@ -26,15 +27,19 @@
 // swizzle, loaded by TMA), and the accumulator holds Y^T (TMEM lane = weight
 // row, column = activation row).
 //
-// Warp roles: warp 0 is the producer (lane 0 issues the TMA loads of the
-// activation and packed-weight tiles, all lanes copy the block scales with
-// cp.async); warp 1 allocates TMEM and lane 0 issues the MMAs; the remaining
-// warps are converters, 4 x KS x RS of them: each K-slice of a stage has RS
-// groups of 4 warps (one thread per weight row, each taking 64 / RS of the
-// row's values).  A converter looks each 4-bit code up in a 16-entry bf16
-// codebook held in registers (byte permutes), scales it by the block absmax
-// with one bf16x2 multiply, and stores the values into its TMEM lane with
-// tcgen05.st.  Every wait is bounded (NF4_WAIT_LIMIT_NS); on expiry the CTA
+// Warp roles: warp 0 lane 0 loads the activation tiles (TMA); warp 1
+// allocates TMEM and lane 0 issues the MMAs (narrow tiles add a second
+// issuer warp); the last warp loads the packed-weight tiles (TMA, lane 0)
+// and copies the block scales (cp.async, all lanes); the warps in between
+// are converters, 4 x KS x RS of them: each K-slice of a stage has RS groups
+// of 4 warps (one thread per weight row, each taking 64 / RS of the row's
+// values).  A 16-bit converter looks each 4-bit code up in the codebook of
+// the compute dtype -- held in registers (byte permutes) on the direct path,
+// in a per-lane shared-memory byte table on the split path -- scales it by
+// the block absmax with one paired multiply and stores the values into its
+// TMEM lane with tcgen05.st; an fp32 converter uses a 16-entry fp32 table,
+// an fp32 multiply and rounds to tf32.  The converters then run the
+// epilogue.  Every wait is bounded (NF4_WAIT_LIMIT_NS); on expiry the CTA
 // records an error code, drains what it has in flight and returns.
 #include <algorithm>
 #include <mutex>

@@ -1,9 +1,10 @@
 // nf4_quant.cu -- blockwise absmax NF4 quantizer and byte-LUT dequantizer.
 //
 // Quantizer: diffuseR pull request "Gemma3 NF4 on GPU" (#39), Summary -- the
-// projection weights "pack to NF4".  Dequantizer: same paragraph -- the eager
-// dequant gathers one lookup-table entry per packed byte straight into the
-// output buffer.  Both kernels are HBM-bound streaming kernels.
+// projection weights are packed to NF4.  Dequantizer: same paragraph -- the
+// eager dequant gathers one lookup-table entry per packed byte straight into
+// the output buffer.  Both kernels are HBM-bound streaming kernels; each
+// takes bf16, fp16 or fp32 weights / outputs.
 #include "nf4_device.cuh"
 #include "nf4_launch.h"
 
