@@ -73,13 +73,21 @@ def peaks():
 GEMM_SOURCES = ("nf4_device.cuh", "nf4_gemm.cu", "nf4_launch.h")   # what ts_kernel is built from
 
 
+def code_tokens(text: str) -> str:
+    """C++ source with comments removed and whitespace collapsed: what the
+    compiler sees, so a comment edit does not change the hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources of the kernel the roofline reports (ts_kernel)."""
+    """Hash of the code of the kernel the roofline reports (ts_kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nf4_weight_quantized_quantize_gb300", "csrc")
     for fn in GEMM_SOURCES:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, fn)) as f:
+            h.update(fn.encode() + b"\0" + code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
