@@ -173,3 +173,18 @@ def test_no_device_is_reported_not_crashed():
         pytest.skip("a GPU is present")
     assert nf4.nf4_quantize(FAKE, 128, 64, FAKE, FAKE) == nf4.NF4_ERR_DEVICE
     assert nf4.nf4_last_error(0) == nf4.NF4_ERR_DEVICE
+
+
+def test_tensor_wrappers_refuse_host_tensors_and_wrong_dtypes():
+    """The torch-level wrappers check device, dtype and layout before calling
+    the library (no device needed to see the refusal)."""
+    import torch
+    with pytest.raises(TypeError):
+        nf4.quantize(torch.zeros(128, dtype=torch.bfloat16))          # host tensor
+    with pytest.raises(TypeError):
+        nf4.quantize(torch.zeros(128, dtype=torch.float64))           # not a compute dtype
+    with pytest.raises(TypeError):
+        nf4.dequantize(torch.zeros(64, dtype=torch.uint8), torch.zeros(2, dtype=torch.float32))
+    with pytest.raises(TypeError):
+        nf4.linear(torch.zeros(2, 64, dtype=torch.int32), torch.zeros(32, dtype=torch.uint8),
+                   torch.zeros(1, dtype=torch.float32), 1)
