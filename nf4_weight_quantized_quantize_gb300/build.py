@@ -2,7 +2,7 @@
 
 Each .cu file under csrc/ compiles to an object in parallel (one -gencode:
 compute_103a -> sm_103a), then nvcc links them with the static CUDA runtime
-into ``libnf4.so`` beside this file.  No cmake, no setuptools; the driver API
+into ``libnf4.so`` beside this file.  No cmake, no setuptools; the CUDA driver API
 is reached through cudaGetDriverEntryPointByVersion, so the library has no
 link-time dependency on libcuda and loads on a machine without a GPU.
 

@@ -167,7 +167,7 @@ def test_workspace_size_rules():
 
 def test_no_device_is_reported_not_crashed():
     """With arguments that pass validation and no usable GPU the call returns
-    NF4_ERR_DEVICE (on a GPU machine this test is skipped)."""
+    NF4_ERR_DEVICE (with a GPU present this test is skipped)."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
@@ -188,3 +188,17 @@ def test_tensor_wrappers_refuse_host_tensors_and_wrong_dtypes():
     with pytest.raises(TypeError):
         nf4.linear(torch.zeros(2, 64, dtype=torch.int32), torch.zeros(32, dtype=torch.uint8),
                    torch.zeros(1, dtype=torch.float32), 1)
+
+
+def test_kernel_hash_ignores_comments_and_layout():
+    """The ncu traffic line is keyed to the GEMM code without comments and
+    whitespace: editing a comment keeps it, editing code does not."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    a = "int f(int x) {  // the input\n    return x + 1; /* one */\n}\n"
+    b = "/* header */\nint f(int x) {\n  return x + 1;\n}"
+    assert bench.code_tokens(a) == bench.code_tokens(b) == "int f(int x) { return x + 1; }"
+    assert bench.code_tokens(a) != bench.code_tokens(a.replace("x + 1", "x + 2"))
+    assert len(bench.kernel_source_hash()) == 16
