@@ -190,10 +190,7 @@ __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
 }
 
 constexpr int kQuantThreads = 256;
-#ifndef NF4_QUANT_UNROLL
-#define NF4_QUANT_UNROLL 1
-#endif
-constexpr int kQuantUnroll = NF4_QUANT_UNROLL;   // 16-byte words in flight per thread
+constexpr int kQuantUnroll = 1;   // 16-byte words in flight per thread
 
 // Vectorized quantizer for whole blocks of a 16-bit type DT.  Thread t of a
 // warp owns the 16-byte word t of a 512-byte warp tile (4 blocks); 8 lanes

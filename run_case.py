@@ -1,6 +1,6 @@
 """Run one library call on a named synthetic workload a few times (for profiling).
 
-    python -m nf4_weight_quantized_quantize_gb300.run_case \
+    python run_case.py \
         --workload gemma3_12b_gate_up_m2048 --op linear --iters 3
 
 --op is one of quantize, dequantize, linear, linear_geglu (the workload's
@@ -16,7 +16,7 @@ import os
 import statistics
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -49,7 +49,7 @@ def main(argv=None):
         x = workloads.make_activation(cfg, device=dev, dtype=dt)
         y = torch.empty(cfg.m, cfg.n // 2, dtype=dt, device=dev)
         _, wsb = nf4.nf4_linear_workspace_size(cfg.m, cfg.n, cfg.k)
-        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
         fn = lambda: nf4.linear_geglu(x, packed, absmax, cfg.n // 2, out=y, workspace=ws)  # noqa: E731
     else:
         x = workloads.make_activation(cfg, device=dev, dtype=dt)
