@@ -47,6 +47,11 @@
  *     and exits early; nf4_last_error() reports it.  No call aborts the
  *     process or throws.
  *   - The current CUDA device must be an sm_103 GPU (else NF4_ERR_DEVICE).
+ *   - Per device the library resolves, on its first call there, the device
+ *     addresses of its own __device__ objects (the error word, and the scratch
+ *     array of nf4_linear_noalloc) and caches them for the life of the
+ *     process.  A cudaDeviceReset() discards them: do not call the library on
+ *     a device after resetting it in the same process.
  */
 #ifndef NF4_H_
 #define NF4_H_
@@ -133,13 +138,23 @@ NF4_API nf4_status nf4_dequantize(const uint8_t* packed, const float* absmax, in
  *            rounding at the end
  *   workspace, workspace_bytes  scratch of at least
  *            nf4_linear_workspace_size(M, N, K) bytes (may be NULL when that
- *            size is 0); contents need no initialisation and are clobbered
+ *            size is 0, i.e. M >= 128).  Its first NF4_WORKSPACE_HEADER_BYTES
+ *            bytes are arrival counters of the M <= 16 kernel: they must be
+ *            zero before the workspace's first use, and every call -- one
+ *            that reports NF4_ERR_TIMEOUT included -- leaves them zero again,
+ *            so a workspace zeroed once can be reused for any shape, on one
+ *            stream at a time.  The rest needs no initialisation and is
+ *            clobbered.
  *
  * Requirements: M, N >= 0, K > 0, K % 64 == 0, block == NF4_BLOCK; x, packed, y
- * and workspace 16-byte aligned, absmax 4-byte aligned.  Not bit-exact: the
- * fp32 accumulation order is the kernel's; the result matches an fp64 matmul of
- * the dequantized weights to within bf16 output rounding plus fp32 summation
- * error.  Rows of Y are independent of each other.
+ * and workspace 16-byte aligned, absmax 4-byte aligned.  The weight is the
+ * dequantizer's: each element is bf16_rne(float(bf16(C[code])) * absmax) for
+ * any fp32 absmax (also one that is not a bf16 value, as from a weight
+ * quantized at fp32).  Not bit-exact: the fp32 accumulation order is the
+ * kernel's, but repeated calls on the same inputs give the same bits; the
+ * result matches an fp64 matmul of the dequantized weights to within bf16
+ * output rounding plus fp32 summation error.  Rows of Y are independent of
+ * each other.  After NF4_ERR_TIMEOUT (see nf4_last_error) y is undefined.
  */
 NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
                       const float* absmax, int64_t N, int32_t block, uint16_t* y,
@@ -163,7 +178,8 @@ NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uin
  *   y        [M, F] bf16 bits out, row-major; G in fp32, the activation and
  *            the product in fp32, one bf16 rounding at the end
  *   workspace, workspace_bytes  at least nf4_linear_workspace_size(M, 2F, K)
- *            bytes (NULL allowed when that is 0)
+ *            bytes (NULL allowed when that is 0), with the zeroed counter
+ *            header described at nf4_linear
  *
  * Requirements and errors as for nf4_linear with N = 2F (F < 2^30).  Not
  * bit-exact: matches gelu_tanh(g) * u of an fp64 matmul of the dequantized
@@ -184,12 +200,23 @@ NF4_API nf4_status nf4_linear_geglu(const uint16_t* x, int64_t M, int64_t K, con
  *                    kernel; w must be aligned to its element size.
  * nf4_dequantize_ex  out is [numel] of `dtype`; fp32 output is
  *                    C[code] * absmax in fp32 (4 bytes per element written).
- * nf4_linear_ex,     x and y of `dtype`, bf16 or fp16 (the MMA's operand
- * nf4_linear_geglu_ex  types); fp32 returns NF4_ERR_DTYPE.  For fp16 the
- *                    fused kernels scale fp16 codebook values by the absmax
- *                    rounded to fp16, so they reproduce nf4_dequantize_ex's
- *                    fp16 values exactly when every absmax is an fp16 value
- *                    (true for weights nf4_quantize_ex quantized from fp16).
+ * nf4_linear_ex,     x and y of `dtype`:
+ * nf4_linear_geglu_ex  - bf16, fp16: the weight operand is exactly
+ *                      nf4_dequantize_ex's value of that dtype,
+ *                      DT_rne(float(DT(C[code])) * absmax), for any fp32
+ *                      absmax (the kernels multiply in one paired 16-bit
+ *                      operation when the absmax is itself a DT value, and in
+ *                      fp32 with one rounding otherwise -- so an absmax above
+ *                      fp16's range gives +-inf weights and 0 for code 7, as
+ *                      the dequantizer does); fp32 accumulation, one rounding
+ *                      of Y to DT.
+ *                    - fp32: runs on the tf32 tensor cores.  The weight is
+ *                      C[code] * absmax in fp32 rounded to tf32 (10 fraction
+ *                      bits, to nearest, ties away from zero); the tensor
+ *                      core reads X's values with their fraction truncated to
+ *                      10 bits; fp32 accumulation and fp32 Y, no further
+ *                      rounding.  Each product is within 2^-9 relative of
+ *                      the exact fp32 one.
  *
  * Results, requirements and errors otherwise as the bf16 forms; a dtype
  * outside nf4_dtype returns NF4_ERR_DTYPE.
@@ -206,8 +233,11 @@ NF4_API nf4_status nf4_linear_geglu_ex(const void* x, nf4_dtype dtype, int64_t M
                                        int32_t block, void* y, void* workspace,
                                        size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace nf4_linear needs for this shape (host only, no device
- * call).  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad arguments. */
+/* Bytes of workspace nf4_linear needs for this shape, at any dtype (host
+ * only, no device call): 0 for M >= 128, else at least
+ * NF4_WORKSPACE_HEADER_BYTES.  Returns NF4_ERR_NULL / NF4_ERR_SHAPE on bad
+ * arguments. */
+#define NF4_WORKSPACE_HEADER_BYTES 4096
 NF4_API nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /*
@@ -230,7 +260,9 @@ NF4_API nf4_status nf4_linear_workspace_size(int64_t M, int64_t N, int64_t K, si
  * cudaGetSymbolAddress with that device current): make it before any stream
  * capture.  All calls on a device share the array: calls that overlap on the
  * GPU (other streams, other host threads) race and must be serialised by the
- * caller.  Nothing in the array needs clearing between calls.
+ * caller.  Each call clears the array's counter header on its stream (a
+ * memset, no allocation) before its kernel; the rest needs no clearing.
+ * After NF4_ERR_TIMEOUT y is undefined.
  */
 #define NF4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 NF4_API nf4_status nf4_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,

@@ -231,7 +231,12 @@ def dequantize(packed, absmax, numel: int | None = None, out=None, dtype=None):
 
 
 def linear(x, packed, absmax, n_out: int, out=None, workspace=None):
-    """Y [M, n_out] = X [M, K] . deq(W)^T with W [n_out, K] in NF4; X and Y bf16 or fp16."""
+    """Y [M, n_out] = X [M, K] . deq(W)^T with W [n_out, K] in NF4; X and Y
+    bf16, fp16 or fp32 (fp32 runs on the tf32 tensor cores: X's and the
+    weight's fractions cut to 10 bits, fp32 output).  A given `workspace`
+    (uint8, at least nf4_linear_workspace_size bytes) must start zeroed before
+    its first use; each call leaves its counter header zero again, so it can
+    be reused on one stream.  Without one, a zeroed workspace is allocated."""
     torch = _torch()
     codes = _compute_dtypes()
     _need(x, tuple(codes), "x")
@@ -248,7 +253,7 @@ def linear(x, packed, absmax, n_out: int, out=None, workspace=None):
     st, ws_bytes = nf4_linear_workspace_size(M, n_out, K)
     _check(st, "nf4_linear_workspace_size")
     if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(nf4_linear_ex(x.data_ptr(), codes[x.dtype], M, K, packed.data_ptr(), absmax.data_ptr(), n_out, BLOCK,
@@ -259,7 +264,7 @@ def linear(x, packed, absmax, n_out: int, out=None, workspace=None):
 def linear_geglu(x, packed, absmax, n_ff: int, out=None, workspace=None):
     """Y [M, n_ff] = gelu_tanh(X . Wg^T) * (X . Wu^T), where (packed, absmax)
     is ONE NF4 weight [2 n_ff, K]: the gate rows, then the up rows.  X and Y
-    bf16 or fp16."""
+    bf16, fp16 or fp32 (tf32 tensor cores).  `workspace` as for linear()."""
     torch = _torch()
     codes = _compute_dtypes()
     _need(x, tuple(codes), "x")
@@ -276,7 +281,7 @@ def linear_geglu(x, packed, absmax, n_ff: int, out=None, workspace=None):
     st, ws_bytes = nf4_linear_workspace_size(M, 2 * n_ff, K)
     _check(st, "nf4_linear_workspace_size")
     if ws_bytes and workspace is None:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=x.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(nf4_linear_geglu_ex(x.data_ptr(), codes[x.dtype], M, K, packed.data_ptr(), absmax.data_ptr(), n_ff,

@@ -186,6 +186,70 @@ __device__ __forceinline__ uint32_t scale_entry(uint32_t e, float am) {
     return pack2<DT>(v.x * am, v.y * am);
 }
 
+// ---------------------------------------------------------------- shared arithmetic
+
+// Whether an fp32 absmax is exactly a value of type DT (then one paired DT
+// multiply gives the correctly rounded product).
+template <int DT>
+__device__ __forceinline__ bool exact_in(float am) {
+    if constexpr (DT == kBF16)
+        return (__float_as_uint(am) & 0xffffu) == 0u;
+    else
+        return __half2float(__float2half_rn(am)) == am;
+}
+
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Multiply of two words of two 16-bit values of type DT (bf16 or fp16),
+// one round-to-nearest-even per half.
+template <int DT>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (DT == kBF16)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// GELU, tanh form (Hendrycks and Gimpel, "Gaussian Error Linear Units",
+// section 2): x/2 * (1 + tanh(y)), y = sqrt(2/pi) * (x + 0.044715 x^3), in
+// fp32 through the identity (1 + tanh(y)) / 2 = 1 / (1 + e^(-2y)):
+//   gelu(x) = x / (1 + 2^(x (c0 + c1 x^2))),  c0 = -2 sqrt(2/pi) log2(e),
+//   c1 = 0.044715 c0,
+// with the hardware base-2 exponential and reciprocal (a few 1e-7 relative
+// error; no cancellation, the denominator is at least 1).  For large negative
+// x the power overflows to +inf, its reciprocal is 0 and the result -0, the
+// limit.
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float a = x * fmaf(-0.10294324159622192f, x * x, -2.302208185195923f);
+    float t, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(a));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+    return x * r;
+}
+
+// Element bytes of a compute dtype.
+template <int DT>
+constexpr int elem_bytes() {
+    return DT == kF32 ? 4 : 2;
+}
+
+// Store one output value in the compute dtype (16-bit types: one rounding
+// to nearest even).
+template <int DT>
+__device__ __forceinline__ void store_out(void* y, int64_t i, float v) {
+    if constexpr (DT == kF32)
+        static_cast<float*>(y)[i] = v;
+    else
+        static_cast<uint16_t*>(y)[i] = round16<DT>(v);
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // Wait until the kernel this one was launched after (programmatic dependent

@@ -47,15 +47,13 @@
 
 #include <cudaTypedefs.h>
 
+#include "nf4_convert.cuh"
 #include "nf4_device.cuh"
 #include "nf4_launch.h"
 
 namespace nf4 {
 
 // ============================================================ shared pieces
-
-constexpr int kBK = 64;                    // K per slice = one NF4 block = one 128-byte activation row
-constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per slice
 
 // Barriers, in shared memory.  A stage is KS consecutive K-slices.  Three
 // rings carry it, each as deep as its storage allows:
@@ -89,10 +87,6 @@ struct Barriers {
     __host__ __device__ static constexpr int count(int xs, int ts, int ps) { return xs + 2 * ts + 2 * ps + 3; }
 };
 
-// pfull[p] completes on the TMA bytes plus kPfullArrivals arrivals: the
-// weight producer lane's expect-tx arrive and one cp.async arrive per lane.
-constexpr int kPfullArrivals = 1 + 32;
-
 __device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arrivals, int mma_issuers) {
     for (int s = 0; s < bar.nx; ++s) mbar_init(bar.xfull(s), 1);
     for (int t = 0; t < bar.nt; ++t) {
@@ -106,87 +100,6 @@ __device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arri
     mbar_init(bar.accum(), mma_issuers);
     mbar_init(bar.drain(0), 1);
     mbar_init(bar.drain(1), 1);
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-// Multiply of two words of two 16-bit values of type DT (bf16 or fp16),
-// one round-to-nearest-even per half.
-template <int DT>
-__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    if constexpr (DT == kBF16)
-        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    else
-        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// The 16 codebook values of type DT split into low bytes (l) and high bytes
-// (h), four codes per register: byte i of l[q] is the low byte of DT(C[4q + i]).
-struct CodebookRegs {
-    uint32_t l[4], h[4];
-};
-
-template <int DT>
-__device__ __forceinline__ CodebookRegs codebook_regs() {
-    CodebookRegs cb;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        cb.l[q] = 0;
-        cb.h[q] = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t bits = round16<DT>(c_code[4 * q + i]);
-            cb.l[q] |= (bits & 0xffu) << (8 * i);
-            cb.h[q] |= (bits >> 8) << (8 * i);
-        }
-    }
-    return cb;
-}
-
-// Look up the four codes held in the low 16 bits of s (nibble k = code k).
-// A byte permute picks byte (code & 7) out of eight table bytes; two of them
-// cover codes 0-7 and 8-15, and a third picks per byte by code bit 3.  Byte k
-// of `lo` / `hi` is the low / high byte of bf16(C[code k]).
-__device__ __forceinline__ void lookup4(uint32_t s, const CodebookRegs& cb, uint32_t& lo, uint32_t& hi) {
-    const uint32_t s7 = s & 0x7777u;
-    const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;
-    lo = prmt(prmt(cb.l[0], cb.l[1], s7), prmt(cb.l[2], cb.l[3], s7), pick);
-    hi = prmt(prmt(cb.h[0], cb.h[1], s7), prmt(cb.h[2], cb.h[3], s7), pick);
-}
-
-// One packed word (bytes in address order; byte j holds code 2j in its high
-// nibble) to four words of two DT values, element 2i in the low half of word
-// i, each scaled by `am2`.  A product of two bf16 (or two fp16) values is
-// exact in fp32, so each value is DT_rne(float(DT(C)) * absmax) -- the
-// dequantizer's value -- whenever absmax is a DT value, which every absmax
-// nf4_quantize writes for a DT weight is (the max of DT magnitudes).
-template <int DT>
-__device__ __forceinline__ void expand8(uint32_t p, const CodebookRegs& cb, uint32_t am2, uint32_t* o) {
-    uint32_t lo, hi;
-    lookup4(p, cb, lo, hi);              // nibbles: code1, code0, code3, code2
-    o[0] = mul2<DT>(prmt(lo, hi, 0x4051u), am2);
-    o[1] = mul2<DT>(prmt(lo, hi, 0x6273u), am2);
-    lookup4(p >> 16, cb, lo, hi);        // code5, code4, code7, code6
-    o[2] = mul2<DT>(prmt(lo, hi, 0x4051u), am2);
-    o[3] = mul2<DT>(prmt(lo, hi, 0x6273u), am2);
-}
-
-// expand8 through the shared-memory byte table instead of register permutes:
-// per packed byte one table load (the DT codebook values of its two codes,
-// element 2i in the low half) and one paired multiply.  `lut_lane` points at
-// this lane's column of the replicated table (entry b at lut_lane[32 b]).
-template <int DT>
-__device__ __forceinline__ void expand8_lut(uint32_t p, const uint32_t* lut_lane, uint32_t am2, uint32_t* o) {
-    o[0] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4440u)], am2);
-    o[1] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4441u)], am2);
-    o[2] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4442u)], am2);
-    o[3] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4443u)], am2);
 }
 
 // Whether a converter warp reports stage st as converted.  Always true in
@@ -203,72 +116,12 @@ __device__ __forceinline__ bool report_converted(int st) {
 #endif
 }
 
-// Wait (bounded) for the copies a producer issued into the last `slots`
-// stages of its ring to land, so no TMA or cp.async write targets shared
-// memory after exit.
-__device__ __forceinline__ void drain_ring(uint32_t bar0, int slots, int issued, uint32_t* err) {
-    int dummy = 0;   // a fresh flag: the CTA-wide abort is already raised here
-    for (int st = max(0, issued - slots); st < issued; ++st)
-        if (!mbar_wait(bar0 + 8u * (st % slots), (st / slots) & 1, err, &dummy, kErrTimeoutDrain)) break;
-}
-
 // Error-path exit of an MMA issuer: wait (bounded) until every MMA it issued
 // has completed, so TMEM can be released.
 __device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint32_t* err) {
     int dummy = 0;
     mma_commit(bar.drain(issuer));
     mbar_wait(bar.drain(issuer), 0, err, &dummy, kErrTimeoutDrain);
-}
-
-// Weight producer warp, one stage: lane 0 arms pfull[p] with the TMA byte
-// count and loads the packed tile of the whole stage -- one box of 32 * KS
-// bytes x ROWS rows from weight row n0, or, for a gate/up PAIR, two boxes of
-// ROWS / 2 rows from rows n0 (gate) and n1 (up) -- and every lane copies
-// scales with 4-byte cp.async -- K-slice h, rows lane, lane + 32, ... to
-// am_dst[h][row] -- and arrives on pfull[p] when its copies land.  Rows of a
-// box at or past n_lim (the rows of one half) and K-slices past the weight's
-// last block copy a harmless in-range scale (their products are never stored
-// or multiply zeros).
-template <int ROWS, int KS, bool PAIR>
-__device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_t tx_bytes, const CUtensorMap* tm_w,
-                                                uint32_t p_dst, int p_col0, int n0, int n1, int n_lim,
-                                                uint32_t am_dst, const float* absmax, int am_pitch, int kb_abs0) {
-    constexpr int H = PAIR ? ROWS / 2 : ROWS;   // rows per box
-    if (lane == 0) {
-        mbar_arrive_expect_tx(full, tx_bytes);
-        tma_load_2d(p_dst, tm_w, full, p_col0, n0);
-        if constexpr (PAIR) tma_load_2d(p_dst + H * kPackedRow * KS, tm_w, full, p_col0, n1);
-    }
-#pragma unroll
-    for (int h = 0; h < KS; ++h) {
-        const bool kb_ok = kb_abs0 + h < am_pitch;
-#pragma unroll
-        for (int i = lane; i < ROWS; i += 32) {
-            const int il = i < H ? i : i - H;          // row within its box
-            const int n = (i < H ? n0 : n1) + il;
-            const bool ok = n0 + il < n_lim && kb_ok;
-            const float* src = absmax + (ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0);
-            cp_async_4(am_dst + 4u * (h * ROWS + i), src);
-        }
-    }
-    cp_async_arrive_noinc(full);
-}
-
-// GELU, tanh form (Hendrycks and Gimpel, "Gaussian Error Linear Units",
-// section 2): x/2 * (1 + tanh(y)), y = sqrt(2/pi) * (x + 0.044715 x^3), in
-// fp32 through the identity (1 + tanh(y)) / 2 = 1 / (1 + e^(-2y)):
-//   gelu(x) = x / (1 + 2^(x (c0 + c1 x^2))),  c0 = -2 sqrt(2/pi) log2(e),
-//   c1 = 0.044715 c0,
-// with the hardware base-2 exponential and reciprocal (a few 1e-7 relative
-// error; no cancellation, the denominator is at least 1).  For large negative
-// x the power overflows to +inf, its reciprocal is 0 and the result -0, the
-// limit.
-__device__ __forceinline__ float gelu_tanh(float x) {
-    const float a = x * fmaf(-0.10294324159622192f, x * x, -2.302208185195923f);
-    float t, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(a));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
-    return x * r;
 }
 
 // Named barriers among the converter warps (barrier 0 is __syncthreads).
@@ -297,7 +150,7 @@ __device__ __forceinline__ void converters_sync(int threads) {
 // (MMA N), stages of KS K-slices, RS converter threads per weight row and
 // K-slice (each expands 64 / RS of the row's values), EB bytes per element
 // of X and of the converted weights (2: bf16 / fp16, 4: fp32 read as tf32).
-template <int NX, int KS, int RS, int LUT, int WS, int EB = 2>
+template <int NX, int KS, int RS, int LUT, int EB = 2>
 struct TsCfg {
     static constexpr int BW = 128;                      // weight rows per tile (MMA M)
     static constexpr int XB = NX * kBK * EB;            // activation tile of one K-slice
@@ -307,9 +160,7 @@ struct TsCfg {
     static constexpr int XHALVES = EB / 2;
     static constexpr int XSUB = NX * 128;
     static constexpr int MMAS = kBK * EB / 32;
-    // A weight-ring slot holds WS stages (WS * KS K-slices): the converter
-    // warps wait on it once per WS stages.
-    static constexpr int WK = KS * WS;                  // K-slices per weight slot
+    static constexpr int WK = KS;                       // K-slices per weight slot
     static constexpr int P_BYTES = BW * kPackedRow * WK;
     static constexpr int AM_BYTES = BW * 4 * WK;
     static constexpr int X_SLOT = KS * XB;                               // activation ring slot
@@ -332,11 +183,9 @@ struct TsCfg {
     static constexpr int A_SLOT = A_COLS * KS;
     static constexpr int TMEM_SLOTS = (TMEM_COLS - A_COL0) / A_SLOT;
     static constexpr int SMEM_LIMIT = 232448;
-    // LUT: a 256-entry bf16x2 byte table replicated once per lane (entry b of
-    // lane l at word 32 b + l, so a warp's lookups never share a bank)
-    // (LUT == 1: every converter warp uses it; LUT == 2: the warps of row
-    // part 1 use it and those of part 0 the register permutes, splitting the
-    // expansion between the shared-memory and ALU pipes)
+    // LUT == 1: the converters expand through a 256-entry byte table
+    // replicated once per lane (entry b of lane l at word 32 b + l, so a
+    // warp's lookups never share a bank); LUT == 0: through register permutes
     static constexpr int LUT_BYTES = LUT != 0 ? 256 * 32 * 4 : 0;
     static constexpr int BUDGET = SMEM_LIMIT - 2048 - LUT_BYTES;   // alignment slack, barriers
     static constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -368,6 +217,7 @@ struct TsCfg {
     static_assert(SX >= 2 && ST >= SX && SP >= 3, "ring depths");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
     static_assert(WK == 1 || WK == 2 || WK == 4, "packed rows of 32, 64 or 128 bytes");
+    static_assert(LUT == 0 || LUT == 1, "expansion through permutes or the byte table");
     static_assert(RS == 1 || RS == 2, "converter threads per row");
     static_assert(EB == 2 || (EB == 4 && LUT == 0), "fp32 expands through the 16-entry code table");
     // The packed tile is loaded with the TMA swizzle whose span equals its
@@ -393,22 +243,6 @@ struct TsArgs {
     uint32_t* err;
 };
 
-// Element bytes of a compute dtype.
-template <int DT>
-constexpr int elem_bytes() {
-    return DT == kF32 ? 4 : 2;
-}
-
-// Store one output value in the compute dtype (16-bit types: one rounding
-// to nearest even).
-template <int DT>
-__device__ __forceinline__ void store_out(void* y, int64_t i, float v) {
-    if constexpr (DT == kF32)
-        static_cast<float*>(y)[i] = v;
-    else
-        static_cast<uint16_t*>(y)[i] = round16<DT>(v);
-}
-
 // fp32 weights: one packed word (bytes in address order, code 2j in the high
 // nibble of byte j) to eight values C[code] * absmax in fp32 -- the fp32
 // dequantizer's values -- rounded to tf32, the part the MMA reads.
@@ -423,11 +257,11 @@ __device__ __forceinline__ void expand8_f32(uint32_t p, const float* code, float
 
 // DT: the compute dtype of X, Y and the converted weights: bf16 or fp16
 // (kind::f16) or fp32 (kind::tf32).
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
-__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>::THREADS, 1)
+template <int NX, int KS, int RS, int LUT, bool SPLIT, bool GEGLU, int DT>
+__global__ void __launch_bounds__(TsCfg<NX, KS, RS, LUT, elem_bytes<DT>()>::THREADS, 1)
 ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
           const TsArgs args) {
-    using C = TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>;
+    using C = TsCfg<NX, KS, RS, LUT, elem_bytes<DT>()>;
     static_assert(DT == kBF16 || DT == kF16 || DT == kF32, "compute dtypes");
     static_assert(!(SPLIT && GEGLU), "a gate/up pair sums its split-K partials before the activation");
     // output columns per tile: 128 weight rows, or 64 gate/up row pairs
@@ -458,7 +292,6 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const int kb0 = split * args.kb_per_split;
     const int nk = min(args.kb_per_split, nk_total - kb0);
     const int nst = (nk + KS - 1) / KS;   // stages; the last may hold fewer than KS K-slices
-    const int nws = (nst + WS - 1) / WS;  // weight-ring stages
 
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::OFF_LUT);
     if constexpr (LUT != 0) {
@@ -515,23 +348,21 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (*abort_flag) drain_ring(bar.xfull(0), SX, issued, args.err);
         }
     } else if (warp == C::WPROD_WARP) {
-        // ---------------- weight producer: refills weight slot p (WS stages)
-        // once every converter warp has read what it held and the MMAs that
-        // last read the TMEM slots of its stages completed -- so pfull alone
-        // tells a converter warp it may go ahead (one barrier wait per WS
-        // stages).  MMAs complete in order: waiting for the last of those
-        // stages' predecessors covers the others.
+        // ---------------- weight producer: refills weight slot p with stage
+        // st once every converter warp has read what the slot held and the MMAs
+        // that last read the stage's TMEM slot completed -- so pfull alone
+        // tells a converter warp it may go ahead (one barrier wait per stage).
         int issued = 0;
-        for (int ws = 0; ws < nws; ++ws) {
-            const int p = ws % SP;
+        for (int st = 0; st < nst; ++st) {
+            const int p = st % SP;
             bool ok = true;
-            if (ws >= SP) ok = mbar_wait(bar.pempty(p), ((ws / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
-            const int prev = min(WS * ws + WS - 1, nst - 1) - ST;   // MMAs of stage `prev` must be done
+            if (st >= SP) ok = mbar_wait(bar.pempty(p), ((st / SP) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty);
+            const int prev = st - ST;   // MMAs of stage `prev` (same TMEM slot) must be done
             if (ok && prev >= 0)
                 ok = mbar_wait(bar.done(prev % ST), (prev / ST) & 1, args.err, abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
-            const int kb = kb0 + ws * C::WK;
-            produce_weights<C::BW, C::WK, GEGLU>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
+            const int kb = kb0 + st * KS;
+            produce_weights<C::BW, KS, GEGLU>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
                                                  kb * kPackedRow, n0, args.N + n0, args.N, smem_u32(am_tile(p)),
                                                  args.absmax, nk_total, kb);
             ++issued;
@@ -602,99 +433,95 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int r = q * 32 + lane;             // weight row within the tile = TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const CodebookRegs cb = codebook_regs<DT == kF32 ? kBF16 : DT>();
+        constexpr int D16 = DT == kF32 ? kBF16 : DT;   // the 16-bit type (unused for fp32)
         bool ok = true;
-        for (int ws = 0; ws < nws; ++ws) {
-            const int p = ws % SP;
-            // the packed tiles and scales of WS stages; the weight producer
-            // loaded them only after the MMAs that last read their TMEM slots
-            const bool got = mbar_wait(bar.pfull(p), (ws / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
+        for (int st = 0; st < nst; ++st) {
+            const int p = st % SP;
+            const int t = st % ST;
+            // the stage's packed tile and scales; the weight producer loaded
+            // them only after the MMAs that last read TMEM slot t
+            const bool got = mbar_wait(bar.pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // read this thread's share of every stage of the slot, then free it
+            // read this thread's share of the stage, then free the weight slot
             const uint8_t* ptile = p_tile(p);
-            uint4 q0[WS], q1[WS];
-            float am[WS];
-#pragma unroll
-            for (int w = 0; w < WS; ++w) {
-                const int st = WS * ws + w;
-                const int ks = w * KS + h;                   // K-slice within the weight slot
-                q0[w] = make_uint4(0, 0, 0, 0);
-                q1[w] = make_uint4(0, 0, 0, 0);
-                am[w] = 0.0f;
-                if (st < nst && st * KS + h < nk) {          // warp-uniform
-                    am[w] = am_tile(p)[ks * C::BW + r];
-                    if constexpr (RS == 1) {
-                        q0[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks));
-                        q1[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks + 1));
-                    } else {
-                        q0[w] = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * ks + part));
-                    }
+            const bool live = st * KS + h < nk;           // warp-uniform: the K-slice exists
+            uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+            float am = 0.0f;
+            if (live) {
+                am = am_tile(p)[h * C::BW + r];
+                if constexpr (RS == 1) {
+                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h));
+                    q1 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + 1));
+                } else {
+                    q0 = *reinterpret_cast<const uint4*>(ptile + C::packed_offset(r, 2 * h + part));
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar.pempty(p));   // this warp is done with weight slot p
-#pragma unroll
-            for (int w = 0; w < WS; ++w) {
-                const int st = WS * ws + w;
-                if (st >= nst) break;
-                const int t = st % ST;
-                if (DT == kF32 && st * KS + h < nk) {        // warp-uniform
-                    // 64 fp32 values per row and K-slice: 64 TMEM columns
-                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + C::A_COLS * h;
-                    uint32_t v[32];
-                    expand8_f32(q0[w].x, code_f32, am[w], v + 0);
-                    expand8_f32(q0[w].y, code_f32, am[w], v + 8);
-                    expand8_f32(q0[w].z, code_f32, am[w], v + 16);
-                    expand8_f32(q0[w].w, code_f32, am[w], v + 24);
-                    tmem_st32(col + 32 * (RS == 1 ? 0 : part), v);
-                    if constexpr (RS == 1) {
-                        expand8_f32(q1[w].x, code_f32, am[w], v + 0);
-                        expand8_f32(q1[w].y, code_f32, am[w], v + 8);
-                        expand8_f32(q1[w].z, code_f32, am[w], v + 16);
-                        expand8_f32(q1[w].w, code_f32, am[w], v + 24);
-                        tmem_st32(col + 32, v);
-                    }
-                    tmem_st_wait();
-                } else if (DT != kF32 && st * KS + h < nk) {   // warp-uniform
-                    const uint32_t am2 = pack2<DT == kF32 ? kBF16 : DT>(am[w], am[w]);
-                    const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + C::A_COLS * h;
-                    const uint32_t* lut_lane = lut + lane;
-                    constexpr int D16 = DT == kF32 ? kBF16 : DT;
-                    auto expand = [&](uint32_t word, uint32_t* o) {
-                        if (LUT == 1 || (LUT == 2 && part == 1))   // warp-uniform
-                            expand8_lut<D16>(word, lut_lane, am2, o);
-                        else
-                            expand8<D16>(word, cb, am2, o);
-                    };
-                    if constexpr (RS == 1) {
-                        uint32_t v[32];
-                        expand(q0[w].x, v + 0);
-                        expand(q0[w].y, v + 4);
-                        expand(q0[w].z, v + 8);
-                        expand(q0[w].w, v + 12);
-                        expand(q1[w].x, v + 16);
-                        expand(q1[w].y, v + 20);
-                        expand(q1[w].z, v + 24);
-                        expand(q1[w].w, v + 28);
-                        tmem_st32(col, v);
-                    } else {
-                        // 16 packed bytes = 32 values = 16 TMEM columns
-                        uint32_t v[16];
-                        expand(q0[w].x, v + 0);
-                        expand(q0[w].y, v + 4);
-                        expand(q0[w].z, v + 8);
-                        expand(q0[w].w, v + 12);
-                        tmem_st16(col + 16 * part, v);
-                    }
-                    tmem_st_wait();
+            const uint32_t col = lane_addr + C::A_COL0 + t * C::A_SLOT + C::A_COLS * h;
+            if (DT == kF32 && live) {
+                // 64 fp32 values per row and K-slice: 64 TMEM columns
+                uint32_t v[32];
+                expand8_f32(q0.x, code_f32, am, v + 0);
+                expand8_f32(q0.y, code_f32, am, v + 8);
+                expand8_f32(q0.z, code_f32, am, v + 16);
+                expand8_f32(q0.w, code_f32, am, v + 24);
+                tmem_st32(col + 32 * (RS == 1 ? 0 : part), v);
+                if constexpr (RS == 1) {
+                    expand8_f32(q1.x, code_f32, am, v + 0);
+                    expand8_f32(q1.y, code_f32, am, v + 8);
+                    expand8_f32(q1.z, code_f32, am, v + 16);
+                    expand8_f32(q1.w, code_f32, am, v + 24);
+                    tmem_st32(col + 32, v);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(t));
+                tmem_st_wait();
+            } else if (DT != kF32 && live) {
+                const uint32_t* lut_lane = lut + lane;
+                // An absmax that is a D16 value scales in one paired D16 multiply
+                // (exact product, one rounding); any other absmax (a weight
+                // quantized at another dtype) scales each value in fp32 and
+                // rounds once -- the dequantizer's value either way.
+                const bool exact = exact_in<D16>(am);
+                const uint32_t am2 = exact ? pack2<D16>(am, am) : pack2<D16>(1.0f, 1.0f);
+                auto expand = [&](uint32_t word, uint32_t* o) {
+                    if constexpr (LUT == 1)
+                        expand8_lut<D16>(word, lut_lane, am2, o);
+                    else
+                        expand8<D16>(word, cb, am2, o);
+                    if (!exact) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = scale_entry<D16>(o[i], am);
+                    }
+                };
+                if constexpr (RS == 1) {
+                    uint32_t v[32];
+                    expand(q0.x, v + 0);
+                    expand(q0.y, v + 4);
+                    expand(q0.z, v + 8);
+                    expand(q0.w, v + 12);
+                    expand(q1.x, v + 16);
+                    expand(q1.y, v + 20);
+                    expand(q1.z, v + 24);
+                    expand(q1.w, v + 28);
+                    tmem_st32(col, v);
+                } else {
+                    // 16 packed bytes = 32 values = 16 TMEM columns
+                    uint32_t v[16];
+                    expand(q0.x, v + 0);
+                    expand(q0.y, v + 4);
+                    expand(q0.z, v + 8);
+                    expand(q0.w, v + 12);
+                    tmem_st16(col + 16 * part, v);
+                }
+                tmem_st_wait();
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && report_converted(st)) mbar_arrive(bar.conv(t));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = ok && mbar_wait(bar.accum(), 0, args.err, abort_flag, kErrTimeoutAccum);
@@ -830,43 +657,9 @@ __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int spl
     }
 }
 
-// ============================================================ host side
+// ============================================================ host helpers shared with the other kernels
 
 namespace {
-
-constexpr int kTargetCtas = 152;             // one wave on a GB300 (152 SMs)
-#ifndef NF4_KS_DIRECT
-#define NF4_KS_DIRECT 2
-#endif
-#ifndef NF4_KS_SPLIT
-#define NF4_KS_SPLIT 4
-#endif
-#ifndef NF4_RS_DIRECT
-#define NF4_RS_DIRECT 2
-#endif
-constexpr int kBW = 128;                     // weight rows per tile
-constexpr int kKsDirect = NF4_KS_DIRECT;     // K-slices per stage, M >= 128
-constexpr int kKsSplit = NF4_KS_SPLIT;       // K-slices per stage, M < 128
-constexpr int kRsDirect = NF4_RS_DIRECT;     // converter threads per weight row, M >= 128
-constexpr int kRsSplit = 1;                  // converter threads per weight row, M < 128
-#ifndef NF4_LUT_DIRECT
-#define NF4_LUT_DIRECT 0
-#endif
-#ifndef NF4_LUT_SPLIT
-#define NF4_LUT_SPLIT 1
-#endif
-constexpr int kLutDirect = NF4_LUT_DIRECT;   // 1: shared-memory byte table instead of register permutes, 2: half each
-constexpr int kLutSplit = NF4_LUT_SPLIT;
-#ifndef NF4_WS_DIRECT
-#define NF4_WS_DIRECT 1
-#endif
-constexpr int kWsDirect = NF4_WS_DIRECT;     // stages per weight-ring slot, M >= 128
-constexpr int kWsSplit = 1;                  // stages per weight-ring slot, M < 128
-// fp32 (tf32 MMA): activation tiles twice as large, so fewer K-slices per
-// stage; the 16-entry fp32 code table instead of the byte tables.
-constexpr int kKsDirectF32 = 1, kRsDirectF32 = 2;
-constexpr int kKsSplitF32 = 2, kRsSplitF32 = 1;
-static_assert(kKsSplit % kKsSplitF32 == 0, "split-K ranges are whole stages at every dtype");
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -883,6 +676,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+}  // namespace
 
 // 2-D row-major tensor [rows, cols] of `elem` bytes per element, box
 // {box_cols, box_rows}, the given shared-memory swizzle; out-of-range reads fill 0.
@@ -918,6 +713,24 @@ cudaError_t set_smem(const void* kernel, size_t bytes, int device) {
     return e;
 }
 
+// ============================================================ host side
+
+namespace {
+
+constexpr int kTargetCtas = 152;             // one wave on a GB300 (152 SMs)
+constexpr int kBW = 128;            // weight rows per tile
+constexpr int kKsDirect = 2;        // K-slices per stage, M >= 128
+constexpr int kKsSplit = 4;         // K-slices per stage, M < 128
+constexpr int kRsDirect = 2;        // converter threads per weight row, M >= 128
+constexpr int kRsSplit = 1;         // converter threads per weight row, M < 128
+constexpr int kLutDirect = 0;       // M >= 128: register permutes (the byte table costs an activation slot)
+constexpr int kLutSplit = 1;        // M < 128: the per-lane byte table (shared memory is idle there)
+// fp32 (tf32 MMA): activation tiles twice as large, so fewer K-slices per
+// stage; the 16-entry fp32 code table instead of the byte tables.
+constexpr int kKsDirectF32 = 1, kRsDirectF32 = 2;
+constexpr int kKsSplitF32 = 2, kRsSplitF32 = 1;
+static_assert(kKsSplit % kKsSplitF32 == 0, "split-K ranges are whole stages at every dtype");
+
 // How a call is cut into CTAs: a pure function of the shape, so the
 // workspace size needs no device query.
 struct Plan {
@@ -951,12 +764,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K) {
     return p;
 }
 
-template <int NX, int KS, int RS, int LUT, int WS, bool SPLIT, bool GEGLU, int DT>
+template <int NX, int KS, int RS, int LUT, bool SPLIT, bool GEGLU, int DT>
 cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                       const TsArgs& a, cudaStream_t s) {
-    using C = TsCfg<NX, KS, RS, LUT, WS, elem_bytes<DT>()>;
+    using C = TsCfg<NX, KS, RS, LUT, elem_bytes<DT>()>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = ts_kernel<NX, KS, RS, LUT, WS, SPLIT, GEGLU, DT>;
+    auto kernel = ts_kernel<NX, KS, RS, LUT, SPLIT, GEGLU, DT>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -968,32 +781,32 @@ cudaError_t launch_ts(const DeviceInfo& dev, const Plan& p, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-template <bool SPLIT, int KS, int RS, int LUT, int WS, bool GEGLU, int DT>
+template <bool SPLIT, int KS, int RS, int LUT, bool GEGLU, int DT>
 cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                         const TsArgs& a, cudaStream_t s) {
     if constexpr (SPLIT) {
         switch (p.nx) {   // M < 128
-            case 16: return launch_ts<16, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 32: return launch_ts<32, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 48: return launch_ts<48, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 64: return launch_ts<64, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 80: return launch_ts<80, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 96: return launch_ts<96, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 112: return launch_ts<112, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 16: return launch_ts<16, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 32: return launch_ts<32, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 48: return launch_ts<48, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 64: return launch_ts<64, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 80: return launch_ts<80, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 96: return launch_ts<96, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 112: return launch_ts<112, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, SPLIT, false, DT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.nx) {   // 128 <= rows per tile <= 256
-            case 128: return launch_ts<128, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 144: return launch_ts<144, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 160: return launch_ts<160, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 176: return launch_ts<176, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 192: return launch_ts<192, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 208: return launch_ts<208, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 224: return launch_ts<224, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 240: return launch_ts<240, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
-            case 256: return launch_ts<256, KS, RS, LUT, WS, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 128: return launch_ts<128, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 144: return launch_ts<144, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 160: return launch_ts<160, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 176: return launch_ts<176, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 192: return launch_ts<192, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 208: return launch_ts<208, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 224: return launch_ts<224, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 240: return launch_ts<240, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
+            case 256: return launch_ts<256, KS, RS, LUT, SPLIT, GEGLU, DT>(dev, p, tm_x, tm_w, a, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -1008,8 +821,7 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const v
     if (pair && (p.split || N % 2 != 0)) return cudaErrorInvalidValue;
     CUtensorMap tm_x, tm_w;
     constexpr bool F32 = DT == kF32;
-    const int ks = p.split ? (F32 ? kKsSplitF32 : kKsSplit) * kWsSplit
-                           : (F32 ? kKsDirectF32 : kKsDirect) * kWsDirect;   // K-slices per weight slot
+    const int ks = p.split ? (F32 ? kKsSplitF32 : kKsSplit) : (F32 ? kKsDirectF32 : kKsDirect);   // K-slices per stage
     // the packed box row is 32 * ks bytes; its swizzle span matches (TsCfg::packed_offset)
     const CUtensorMapSwizzle wsw = ks == 1 ? CU_TENSOR_MAP_SWIZZLE_32B
                                  : ks == 2 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -1027,14 +839,14 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const v
              p.kb_per_split, p.m_tiles, dev.err_word};
     if constexpr (F32) {
         if (p.split)
-            return dispatch_nx<true, kKsSplitF32, kRsSplitF32, 0, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
-        return pair ? dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, 1, true, DT>(dev, p, tm_x, tm_w, a, s)
-                    : dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, 1, false, DT>(dev, p, tm_x, tm_w, a, s);
+            return dispatch_nx<true, kKsSplitF32, kRsSplitF32, 0, false, DT>(dev, p, tm_x, tm_w, a, s);
+        return pair ? dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, true, DT>(dev, p, tm_x, tm_w, a, s)
+                    : dispatch_nx<false, kKsDirectF32, kRsDirectF32, 0, false, DT>(dev, p, tm_x, tm_w, a, s);
     } else {
         if (p.split)
-            return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, kWsSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
-        return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, true, DT>(dev, p, tm_x, tm_w, a, s)
-                    : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, kWsDirect, false, DT>(dev, p, tm_x, tm_w, a, s);
+            return dispatch_nx<true, kKsSplit, kRsSplit, kLutSplit, false, DT>(dev, p, tm_x, tm_w, a, s);
+        return pair ? dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, true, DT>(dev, p, tm_x, tm_w, a, s)
+                    : dispatch_nx<false, kKsDirect, kRsDirect, kLutDirect, false, DT>(dev, p, tm_x, tm_w, a, s);
     }
 }
 
@@ -1053,6 +865,7 @@ cudaError_t with_dt(int dtype, Fn&& fn) {
 
 cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
+    if (wide_applies(dtype, M, N)) return launch_gemm_wide(dev, dtype, x, M, K, packed, absmax, N, y, s);
     const Plan p = make_plan(M, N, K);
     if (p.split) return cudaErrorInvalidValue;
     return with_dt(dtype, [&](auto dt) {
@@ -1070,9 +883,19 @@ cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, i
     });
 }
 
-size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K) {
+// The tcgen05 split-K path's fp32 partials, [splits, M, N].
+static size_t split_partials_bytes(int64_t M, int64_t N, int64_t K) {
     const Plan p = make_plan(M, N, K);
     return static_cast<size_t>(p.splits) * M * N * sizeof(float);
+}
+
+// Every skinny workspace starts with the warp-MMA kernel's arrival counters
+// (gemv_header_bytes(), zero between calls); the split-K partials of either
+// path follow, so one workspace serves every dtype.
+size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K) {
+    const size_t gv = gemv_workspace_bytes(M, N, K);
+    const size_t split = gemv_header_bytes() + split_partials_bytes(M, N, K);
+    return gv > split ? gv : split;
 }
 
 // N: rows of the weight; geglu: the weight is a gate/up pair (N = 2F) and
@@ -1080,9 +903,12 @@ size_t skinny_workspace_bytes(const DeviceInfo*, int64_t M, int64_t N, int64_t K
 cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
                           const uint8_t* packed, const float* absmax, int64_t N, void* y, void* workspace,
                           size_t ws_bytes, cudaStream_t s, bool geglu) {
+    if (ws_bytes < skinny_workspace_bytes(&dev, M, N, K) || (geglu && N % 2 != 0)) return cudaErrorInvalidValue;
+    if (gemv_applies(dtype, M, N, K))   // M <= 16, bf16 or fp16: warp-MMA kernel, reduction fused
+        return launch_gemv(dev, dtype, x, M, K, packed, absmax, N, y, workspace, ws_bytes, s, geglu);
     const Plan p = make_plan(M, N, K);
-    if (!p.split || ws_bytes < skinny_workspace_bytes(&dev, M, N, K) || (geglu && N % 2 != 0))
-        return cudaErrorInvalidValue;
+    if (!p.split) return cudaErrorInvalidValue;
+    workspace = static_cast<uint8_t*>(workspace) + gemv_header_bytes();   // the counters stay untouched
     return with_dt(dtype, [&](auto dtc) {
         constexpr int DT = decltype(dtc)::value;
         if (cudaError_t e =

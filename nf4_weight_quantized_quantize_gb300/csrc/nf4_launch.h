@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <utility>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nf4 {
@@ -40,6 +41,16 @@ struct DeviceInfo {
     uint32_t* err_word = nullptr;  // device address of this device's error word
 };
 
+// 2-D row-major tensor map over [rows, cols] elements of `elem` bytes, box
+// {box_cols, box_rows}, the given shared-memory swizzle; reads outside the
+// tensor fill zeros.  False if the driver entry point is missing or the
+// encoding is refused.
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem, uint64_t rows,
+              uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
+
+// Raise a kernel's dynamic shared memory limit, once per (kernel, device).
+cudaError_t set_smem(const void* kernel, size_t bytes, int device);
+
 // Add n to the process-wide count of enqueued kernels (nf4_launch_count).
 void count_launches(int n);
 
@@ -60,6 +71,14 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t
                         const uint8_t* packed, const float* absmax, int64_t N, void* y,
                         cudaStream_t s);
 
+// The wide NF4 GEMM (nf4_gemm_wide.cu): expanded weights in shared memory,
+// two TMEM accumulators, tiles of 128 weight rows x up to 512 activation
+// rows (bf16 / fp16, M > 256).  wide_applies: whether it beats the tile
+// kernel on this shape (a shape-only estimate); launch_gemm uses it then.
+bool wide_applies(int dtype, int64_t M, int64_t N);
+cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                             const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s);
+
 // Workspace bytes the skinny (M < 128) path needs for this shape.
 size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K);
 
@@ -69,8 +88,21 @@ cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, i
                               const uint8_t* packed, const float* absmax, int64_t F, void* y,
                               cudaStream_t s);
 
-// Skinny path: swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an
-// ordered reduction.  N is the weight's row count; with geglu the weight is a
+// Warp-MMA NF4 linear for M <= 16 at bf16 / fp16 (nf4_gemv.cu): whether it
+// takes this shape and dtype, its workspace (a header of arrival counters that
+// must be zero before the first call and is zero again after every call,
+// followed by split-K partials) and its launcher.  rows: the weight's row
+// count (2F for a gate/up pair, whose output is [M, F]).
+bool gemv_applies(int dtype, int64_t M, int64_t rows, int64_t K);
+size_t gemv_workspace_bytes(int64_t M, int64_t rows, int64_t K);
+size_t gemv_header_bytes();
+cudaError_t launch_gemv(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
+                        const uint8_t* packed, const float* absmax, int64_t rows, void* y, void* workspace,
+                        size_t ws_bytes, cudaStream_t s, bool pair);
+
+// Skinny path (M < 128): the warp-MMA kernel where it applies, else the
+// swap-AB tcgen05 GEMM with split-K into an fp32 workspace and an ordered
+// reduction.  N is the weight's row count; with geglu the weight is a
 // gate/up pair (N = 2F) and the reduction writes gelu(gate) * up, [M, F].
 cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
                           const uint8_t* packed, const float* absmax, int64_t N, void* y,

@@ -15,12 +15,14 @@
 // that device current, resolves the real address once with
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls on a device share the one array and it keeps the last
-// call's contents: every element a call reads was written earlier in the
-// same call (each split writes its whole [M, N] slice before the reduction
-// reads it), so nothing needs clearing, but calls that overlap on the GPU
-// (concurrent streams, or host threads) race on it and must be serialised by
-// the caller.  No cudaMalloc, cudaFree or allocating library routine is
-// called here.
+// call's contents.  Its first bytes are the skinny kernel's arrival counters,
+// which must start at zero: each call clears them (a cudaMemsetAsync on the
+// caller's stream, which allocates nothing) before its kernel, so even a call
+// that follows one that timed out starts clean.  Every other element a call
+// reads was written earlier in the same call.  Calls that overlap on the GPU
+// (concurrent streams, or host threads) race on the array and must be
+// serialised by the caller.  No cudaMalloc, cudaFree or allocating library
+// routine is called here.
 #include <mutex>
 
 #include "../../include/nf4.h"
@@ -74,8 +76,13 @@ nf4_status nf4_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, const uin
     if (int st = nf4::current_device_info(&dev); st != NF4_OK) return static_cast<nf4_status>(st);
     void* scratch = nullptr;
     if (nf4_status st = scratch_address(dev->ordinal, &scratch); st != NF4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, nf4::gemv_header_bytes(), s) != cudaSuccess) {
+        cudaGetLastError();
+        return NF4_ERR_CUDA;
+    }
     cudaError_t e = nf4::launch_skinny(*dev, NF4_DTYPE_BF16, x, M, K, packed, absmax, N, y, scratch,
-                                       kNoallocScratchBytes, static_cast<cudaStream_t>(stream));
+                                       kNoallocScratchBytes, s);
     return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 

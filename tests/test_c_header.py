@@ -1,7 +1,7 @@
 """The boundary is a C ABI: include/nf4.h compiles as C11 (gcc, -Wall
 -Werror) and a C program linked against libnf4.so calls it -- version,
-status names, host-side argument checks and the workspace rule -- with no
-GPU and no Python in between."""
+status names, host-side argument checks (fp32 accepted by the linear entry
+points), and the workspace rule -- with no GPU and no Python in between."""
 import os
 import shutil
 import subprocess
@@ -32,6 +32,16 @@ int main(void) {
                             fake, NULL, 0, NULL) != NF4_ERR_BLOCKSIZE) bad |= 32;
     if (nf4_linear_workspace_size(16, 3840, 15360, &ws) != NF4_OK || ws == 0) bad |= 64;
     if (nf4_linear_workspace_size(2048, 3840, 15360, &ws) != NF4_OK || ws != 0) bad |= 128;
+    /* fp32 is a compute dtype of the linear (tf32 tensor cores): accepted, and
+       M = 0 enqueues nothing; a value outside nf4_dtype is refused */
+    if (nf4_linear_ex(fake, NF4_DTYPE_F32, 0, 128, (const uint8_t*)fake, (const float*)fake, 64, NF4_BLOCK,
+                      fake, NULL, 0, NULL) != NF4_OK) bad |= 256;
+    if (nf4_linear_geglu_ex(fake, NF4_DTYPE_F32, 0, 128, (const uint8_t*)fake, (const float*)fake, 32,
+                            NF4_BLOCK, fake, NULL, 0, NULL) != NF4_OK) bad |= 512;
+    if (nf4_linear_ex(fake, (nf4_dtype)3, 0, 128, (const uint8_t*)fake, (const float*)fake, 64, NF4_BLOCK,
+                      fake, NULL, 0, NULL) != NF4_ERR_DTYPE) bad |= 1024;
+    /* every skinny workspace carries the counter header */
+    if (nf4_linear_workspace_size(1, 64, 64, &ws) != NF4_OK || ws < NF4_WORKSPACE_HEADER_BYTES) bad |= 2048;
     printf("%d\n", bad);
     return bad != 0;
 }

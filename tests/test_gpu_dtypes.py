@@ -162,6 +162,33 @@ def test_linear_geglu_f16(M):
                      lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f16"))
 
 
+@pytest.mark.parametrize("M", [16, 64, 300], ids=["warp_mma", "split_tcgen05", "tile_tcgen05"])
+def test_linear_f16_on_weights_quantized_at_f32(M):
+    """The fp16 linear on a weight quantized from fp32 values: its absmax
+    values are not fp16 values, and every 7th row is scaled so that the
+    dequantized values land in fp16's subnormal range.  Every fused kernel
+    must scale by the fp32 absmax and round once (the fp16 dequantizer's
+    value, which the oracle uses) rather than round the absmax first."""
+    N, K = 256, 1024
+    rs = np.random.default_rng(40 + M)
+    w = (rs.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[::7] *= 1e-3
+    p, a = oracle.quantize(w, dtype="f32")
+    assert np.any(a.astype(np.float16).astype(np.float32) != a)
+    x = rand_w(M * K, 1.0, 50 + M, "f16").reshape(M, K)
+    y = nf4.linear(x.to(DEV), torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV), N)
+    torch.cuda.synchronize()
+    yg = y.float().cpu().numpy().astype(np.float64)
+    xb = workloads.host(x)
+    yref = oracle.linear(xb, p, a, N, dtype="f16")
+    nrm = np.linalg.norm(yref, axis=1, keepdims=True)
+    assert float(np.max(np.abs(yg - yref) / nrm)) <= TOL
+    wd = oracle.dequantize(p, a, N * K, dtype="f16").view(np.float16).astype(np.float64).reshape(N, K)
+    mag = np.abs(xb.view(np.float16).astype(np.float64)) @ np.abs(wd).T
+    bound = 2.0 ** -11 * np.abs(yref) + K * 2.0 ** -23 * mag + 2.0 ** -24
+    assert not (np.abs(yg - yref) > bound).any()
+
+
 def test_f16_matches_bf16_path_on_shared_values():
     """Weights and activations exactly representable in both 16-bit types
     (small integers times powers of two): the fp16 and bf16 GEMMs agree to

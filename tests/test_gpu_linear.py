@@ -152,6 +152,23 @@ def test_tile_path_larger_shapes(M, N, K):
     assert np.array_equal(y1, y2)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1000, 10000, 192),    # ragged M (the second accumulator half past M) and N, an odd block count
+    (2047, 4100, 320),     # 4 tiles of 512 rows, the last one ragged; a partial weight tile
+    (4096, 2048, 128),     # 8 tiles of 512 rows, one stage
+])
+def test_wide_path_shapes(M, N, K):
+    """Shapes the two-accumulator kernel takes (expanded weights in shared
+    memory, tiles of 128 x 512): against the oracle on sampled rows, plus
+    determinism."""
+    q = Quantized(rand_bits((N, K), 0.02, M + 5 * N))
+    x_bits = rand_bits((M, K), 1.0, K + 2 * M)
+    rows = np.sort(np.random.default_rng(M + 1).choice(M, 48, replace=False))
+    rows[-1] = M - 1
+    y1, _ = check(x_bits, q, rows=rows)
+    assert np.array_equal(y1, run_linear(x_bits, q))
+
+
 @pytest.mark.parametrize("M", [1, 2, 7, 15, 16, 17, 31, 33, 48, 64, 65, 100, 112, 127])
 def test_skinny_path_all_widths(M):
     N, K = 640, 1536
@@ -204,20 +221,68 @@ def test_matches_cublas_on_dequantized_weight():
     assert frac_bad < 1e-3, frac_bad
 
 
-def test_workspace_reuse_and_user_workspace():
-    N, K, M = 512, 2048, 16
+HEADER = 4096   # the skinny workspace's arrival counters: zero before a call, zero after it
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_workspace_reuse_and_user_workspace(M):
+    """A caller's workspace: zeroed once, then reused.  Every call leaves the
+    counter header zero again (on both skinny kernels); the rest of it may hold
+    anything (filled with 0xFF here) -- the partials are written before they
+    are read.  Too small a workspace is refused before any launch."""
+    N, K = 512, 2048
     q = Quantized(rand_bits((N, K), 0.02, 9))
-    x = workloads.from_bits(rand_bits((M, K), 1.0, 10), DEV)
+    x_bits = rand_bits((M, K), 1.0, 10)
+    x = workloads.from_bits(x_bits, DEV)
     st, need = nf4.nf4_linear_workspace_size(M, N, K)
-    assert st == nf4.NF4_OK and need > 0
-    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)   # garbage contents are fine
+    assert st == nf4.NF4_OK and need > HEADER
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    ws[:HEADER] = 0
     y1 = nf4.linear(x, q.pd, q.ad, N, workspace=ws)
     y2 = nf4.linear(x, q.pd, q.ad, N, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+    assert int(ws[:HEADER].count_nonzero()) == 0
+    yref = oracle.linear(x_bits, q.p, q.a, N)
+    assert row_err(y1.float().cpu().numpy().astype(np.float64), yref) <= TOL
     small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
     with pytest.raises(nf4.NF4Error):
         nf4.linear(x, q.pd, q.ad, N, workspace=small)
+
+
+# ---------------------------------------------------------------- the M <= 16 warp-MMA kernel
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (16, 1000, 64 * 37),    # ragged N, odd block count: a partial last stage, K split
+    (5, 40000, 256),        # more tiles than SMs: two waves, no K split
+    (8, 2048, 3840),        # k_proj shape, one activation octet
+    (9, 4096, 3840),        # q_proj shape, two octets, ragged rows
+    (16, 640, 64 * 3),      # fewer blocks than a stage
+    (3, 130, 64 * 9),       # a tile larger than the weight
+    (16, 3840, 4096),       # o_proj shape
+    (16, 20480, 512),       # 256-row tiles (the 3-slot ring)
+    (7, 20480, 512),        # 256-row tiles, one activation octet
+])
+def test_small_batch_kernel_shapes(M, N, K):
+    q = Quantized(rand_bits((N, K), 0.02, 11 * M + N))
+    x_bits = rand_bits((M, K), 1.0, M + 3 * K)
+    y1, _ = check(x_bits, q, bound=(N * K <= 1 << 23))
+    assert np.array_equal(y1, run_linear(x_bits, q))     # deterministic: fixed split order
+
+
+@pytest.mark.parametrize("M", [16, 64, 256], ids=["warp_mma", "split_tcgen05", "tile_tcgen05"])
+def test_absmax_not_a_bf16_value(M):
+    """Scales that are not bf16 values (a weight quantized at fp32, then used
+    at bf16): every kernel path must still multiply by the exact fp32 absmax
+    and round once, which is what nf4_dequantize (and the oracle) compute."""
+    N, K = 384, 1024
+    q = Quantized(rand_bits((N, K), 0.02, 21))
+    bumped = (q.a.view(np.uint32) | np.uint32(0x5a5)).view(np.float32)   # low fraction bits set
+    q.a = bumped.copy()
+    q.ad = torch.from_numpy(q.a).to(DEV)
+    q._wdeq = None
+    check(rand_bits((M, K), 1.0, 22), q)
 
 
 def test_no_error_recorded():
@@ -240,7 +305,7 @@ def test_cuda_graph_replay_matches_eager():
     y = torch.empty(256, n, dtype=torch.bfloat16, device=DEV)
     ys = torch.empty(16, n, dtype=torch.bfloat16, device=DEV)
     _, ws_bytes = nf4.nf4_linear_workspace_size(16, n, k)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
 
     def step():
         nf4.quantize(w, out=(p, a))

@@ -1,9 +1,12 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-A test build of the library (-DNF4_TEST_DROP_CONVERTED_ARRIVE, wait limit
-50 ms) withholds the "converted" report for the first K-slice, a flag that
-nothing else sets.  The MMA issuer's wait on it must expire; the CTA must then
-record the error word, drain its in-flight copies, release TMEM and return.
+A test build of the library (-DNF4_TEST_DROP_CONVERTED_ARRIVE
+-DNF4_TEST_DROP_CONSUMED_ARRIVE, wait limit 50 ms) withholds two reports,
+flags that nothing else sets: in the tcgen05 kernels the "converted" report
+for the first K-slice, so the MMA issuer's wait on it expires; in the
+warp-MMA kernel (M <= 16) one warp's "consumed" report for the first ring
+slot, so the producer's wait to refill it expires.  The CTA must then record
+the error word, drain its in-flight copies, release what it holds and return.
 The host sees the launch succeed, nf4_last_error() report NF4_ERR_TIMEOUT
 once (the word is cleared by the read), and the context stays usable: the
 normal library computes a correct result right afterwards.
@@ -26,7 +29,8 @@ DEV = "cuda:0"
 
 @pytest.fixture(scope="module")
 def faulty_lib():
-    path = nf4_build.build(extra=["-DNF4_TEST_DROP_CONVERTED_ARRIVE", "-DNF4_WAIT_LIMIT_NS=50000000ull"],
+    path = nf4_build.build(extra=["-DNF4_TEST_DROP_CONVERTED_ARRIVE", "-DNF4_TEST_DROP_CONSUMED_ARRIVE",
+                                  "-DNF4_WAIT_LIMIT_NS=50000000ull"],
                            out=os.path.join(nf4_build.BUILD, "libnf4_droparrive.so"))
     lib = ctypes.CDLL(path)
     P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
@@ -45,13 +49,21 @@ def _inputs(m, n, k, seed):
     return x.to(DEV), torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV), workloads.bits(x), p, a
 
 
-@pytest.mark.parametrize("m", [256, 64], ids=["tile_kernel", "split_kernel"])
-def test_bounded_wait_expires_and_reports(faulty_lib, m):
-    n, k = 512, 1024
-    x, pd, ad, _, _, _ = _inputs(m, n, k, m)
+@pytest.mark.parametrize("m,n,k", [(256, 512, 1024), (64, 512, 1024), (16, 19456, 1792)],
+                         ids=["tile_kernel", "split_kernel", "warp_mma_kernel"])
+def test_bounded_wait_expires_and_reports(faulty_lib, m, n, k):
+    # warp_mma_kernel: 152 tiles of 128 rows, no K split, 7 stages per CTA --
+    # one more than its 6-slot ring, so the producer must wait for slot 0
+    if m <= 16:
+        rs = np.random.default_rng(5)
+        x = torch.from_numpy(rs.standard_normal((m, k)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+        pd = torch.from_numpy(rs.integers(0, 256, n * k // 2, dtype=np.uint8)).to(DEV)
+        ad = torch.ones(n * k // 64, dtype=torch.float32, device=DEV)
+    else:
+        x, pd, ad, _, _, _ = _inputs(m, n, k, m)
     y = torch.empty(m, n, dtype=torch.bfloat16, device=DEV)
     st, need = nf4.nf4_linear_workspace_size(m, n, k)
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=DEV)
     stream = torch.cuda.current_stream().cuda_stream
     st = faulty_lib.nf4_linear(x.data_ptr(), m, k, pd.data_ptr(), ad.data_ptr(), n, 64, y.data_ptr(),
                                ws.data_ptr(), need, stream)
