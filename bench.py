@@ -53,7 +53,6 @@ FLOPS_PER_STEP = 2 * CFG.m * CFG.n * CFG.k + 2 * SKINNY_M * CFG.n * CFG.k
 BYTES_PER_W_QUANT = 2.5625
 BYTES_PER_W_DEQUANT = 2.5625
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
-CPU_SAMPLE_SECONDS = 10.0       # cpu_baseline: repeat the oracle step for at least this long
 REF_STEP_ROWS = 128             # reference arm: rows of X per step
 
 
@@ -196,10 +195,21 @@ def allreduce_max(value: float, ws: int, device=None) -> float:
     return float(t.item())
 
 
-def aggregate_tflops(flops_per_step: int, steps: int, step_ms_max: float, world: int) -> float:
-    """Whole-job throughput of `world` replicas that each ran `steps` steps,
-    timed by the slowest rank."""
-    return world * flops_per_step * steps / (step_ms_max * 1e-3) / 1e12
+def allreduce_sum(value: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_this_rank: float, step_ms_max: float, ws: int, device=None) -> float:
+    """Whole-job throughput: the FLOPs every rank did (each rank counts its own
+    work; replicas do the same amount on their own prompts), summed over ranks,
+    over the slowest rank's time."""
+    return allreduce_sum(flops_this_rank, ws, device) / (step_ms_max * 1e-3) / 1e12
 
 
 def barrier(ws: int):
@@ -223,19 +233,79 @@ def oracle_sample(rows: int, x_bits, w_bits):
     return 2 * (rows + SKINNY_M) * CFG.n * CFG.k, dt
 
 
-def cpu_baseline(min_seconds: float = CPU_SAMPLE_SECONDS):
-    """The oracle on the whole step (all rows), repeated until `min_seconds` of CPU work."""
+# The oracle per workload, on one core and on all cores: (name, projections,
+# X rows of each projection timed on all cores / on one core, W rows quantized
+# and dequantized on all cores / on one core; None = all).  A sample smaller
+# than the workload is timed and its rate reported as "extrapolated" (the
+# oracle's time is linear in the rows of X and in the weight elements).  The
+# stack is timed on layer 0's seven projections and stands for all 48.
+CPU_CASES = (
+    ("tiny", [workloads.TINY], (None, None), (None, None)),
+    ("q_proj_m2048", [workloads.Q_PROJ], (None, 64), (None, None)),
+    ("gate_up_m2048", [workloads.GATE_UP], (256, 16), (None, 4096)),
+    ("down_proj_m2048", [workloads.DOWN], (256, 32), (None, None)),
+    ("down_proj_m16", [workloads.DOWN_SKINNY], (None, None), (None, None)),
+    ("stack_48x7_m8192", [workloads.stack_layer(0, i) for i in range(len(workloads.PROJECTIONS))],
+     (64, 4), (None, 1024)),
+)
+
+
+def _oracle_case(inputs, lin_rows, w_rows, threads):
+    """Time the oracle's quantize, dequantize and linear on the given samples
+    of each projection's (config, W bits, X bits) with `threads` OpenMP
+    threads; rates, and whether they were measured on less than the whole
+    workload."""
     import oracle
-    w = workloads.bits(workloads.make_weight(CFG))
-    x = workloads.bits(workloads.make_activation(CFG))
-    flops, secs, reps = 0, 0.0, 0
-    while secs < min_seconds:
-        f, dt = oracle_sample(CFG.m, x, w)
-        flops, secs, reps = flops + f, secs + dt, reps + 1
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": (f"{reps} x the whole step (quantize + dequantize of W [{CFG.n}, {CFG.k}], linear on all "
-                       f"{CFG.m} rows of X and on the {SKINNY_M}-row batch), fp64 accumulation, "
-                       f"{secs:.1f} s")}
+    oracle.set_num_threads(threads)
+    t_q = t_d = t_l = 0.0
+    n_q = flop = 0
+    part = False
+    for c, w, x in inputs:
+        ws = w if w_rows is None or w_rows >= c.n else w[:w_rows]
+        part |= ws.shape[0] < c.n
+        t0 = time.perf_counter()
+        p, a = oracle.quantize(ws)
+        t_q += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle.dequantize(p, a, ws.size)
+        t_d += time.perf_counter() - t0
+        n_q += ws.size
+        if ws.shape[0] < c.n:
+            p, a = oracle.quantize(w)
+        rows = c.m if lin_rows is None else min(lin_rows, c.m)
+        part |= rows < c.m
+        t0 = time.perf_counter()
+        oracle.linear(x[:rows], p, a, c.n)
+        t_l += time.perf_counter() - t0
+        flop += 2 * rows * c.n * c.k
+    return {"linear_TFLOP/s": flop / t_l / 1e12, "quantize_GB/s": n_q * BYTES_PER_W_QUANT / t_q / 1e9,
+            "dequantize_GB/s": n_q * BYTES_PER_W_DEQUANT / t_d / 1e9, "seconds": t_q + t_d + t_l,
+            "extrapolated": part}
+
+
+def cpu_baseline():
+    """The oracle (fp64 accumulation, plain C) timed on the host cores of this
+    box, per workload, once on one core and once on all cores.  The line's
+    `value` is the headline workload's linear (q_proj, M = 2048) on all cores."""
+    import oracle
+    all_cores = oracle.num_threads()
+    per = {}
+    for name, projs, lin_rows, w_rows in CPU_CASES:
+        inputs = [(c, workloads.bits(workloads.make_weight(c)), workloads.bits(workloads.make_activation(c)))
+                  for c in projs]
+        per[name] = {"all_cores": _oracle_case(inputs, lin_rows[0], w_rows[0], all_cores),
+                     "one_core": _oracle_case(inputs, lin_rows[1], w_rows[1], 1)}
+        del inputs
+        per[name]["samples"] = {"x_rows_all_cores": lin_rows[0], "x_rows_one_core": lin_rows[1],
+                                "w_rows_all_cores": w_rows[0], "w_rows_one_core": w_rows[1]}
+    oracle.set_num_threads(all_cores)
+    secs = sum(v[k]["seconds"] for v in per.values() for k in ("all_cores", "one_core"))
+    head = per["q_proj_m2048"]["all_cores"]
+    return {"value": head["linear_TFLOP/s"], "unit": "TFLOP/s", "cores": all_cores, "kind": "oracle",
+            "sample": (f"q_proj linear on all {CFG.m} rows of X, {all_cores} threads; per workload below: "
+                       f"quantize, dequantize and linear on one core and on all cores ({secs:.1f} s of CPU "
+                       "work in all); 'extrapolated' marks a rate measured on a row sample of the workload"),
+            "configs": per}
 
 
 def run_reference(args):
@@ -271,7 +341,7 @@ def run_reference(args):
 def config_block(args):
     return {"workload": CFG.name, "M": CFG.m, "N": CFG.n, "K": CFG.k, "skinny_M": SKINNY_M,
             "block": 64, "absmax": "fp32", "w_dist": "N(0,0.02) bf16", "x_dist": "N(0,1) bf16",
-            "seeds": {"w": CFG.w_seed, "x": CFG.x_seed},
+            "seeds": {"w": CFG.w_seed, "x": f"{CFG.x_seed} + 1000 x rank (each replica its own prompts)"},
             "l2": "flushed before every step: 512 MiB memset, then a 256 MiB read (clean lines)",
             "parallelism": f"replicas{args.gpus}"}
 
@@ -290,8 +360,9 @@ def run_ours(args):
     import nf4_weight_quantized_quantize_gb300 as nf4
 
     stream = torch.cuda.current_stream(dev)
-    w = workloads.make_weight(CFG, device=dev)
-    x = workloads.make_activation(CFG, device=dev)
+    mine = workloads.for_replica(CFG, rank)    # this replica's prompts, the shared weight
+    w = workloads.make_weight(mine, device=dev)
+    x = workloads.make_activation(mine, device=dev)
     xs = x[:SKINNY_M].contiguous()
     numel = w.numel()
     packed = torch.empty(numel // 2, dtype=torch.uint8, device=dev)
@@ -301,7 +372,7 @@ def run_ours(args):
     ys = torch.empty(SKINNY_M, CFG.n, dtype=torch.bfloat16, device=dev)
     st, ws_bytes = nf4.nf4_linear_workspace_size(SKINNY_M, CFG.n, CFG.k)
     assert st == nf4.NF4_OK
-    wsp = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    wsp = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_read = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -354,7 +425,7 @@ def run_ours(args):
         raise RuntimeError("a kernel reported a timeout in the timed region")
     step_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     step_ms = allreduce_max(step_ms, ws, dev)
-    value = aggregate_tflops(FLOPS_PER_STEP, args.steps, step_ms, ws)
+    value = aggregate_tflops(FLOPS_PER_STEP * args.steps, step_ms, ws, dev)
 
     # ---- per-call breakdown: a second pass with events around every call
     # (kept out of the timed steps above, whose value they would inflate)
@@ -377,7 +448,7 @@ def run_ours(args):
     x_h = x.cpu().pin_memory()
     sets = [dict(w=torch.empty_like(w), x=torch.empty_like(x), xs=torch.empty_like(xs),
                  packed=torch.empty_like(packed), absmax=torch.empty_like(absmax), wdeq=torch.empty_like(wdeq),
-                 y=torch.empty_like(y), ys=torch.empty_like(ys), ws=torch.empty_like(wsp),
+                 y=torch.empty_like(y), ys=torch.empty_like(ys), ws=torch.zeros_like(wsp),
                  y_h=torch.empty(CFG.m, CFG.n, dtype=torch.bfloat16).pin_memory(),
                  ys_h=torch.empty(SKINNY_M, CFG.n, dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -426,7 +497,7 @@ def run_ours(args):
     if not torch.equal(sets[(args.steps - 1) % 2]["y_h"], y.cpu()):
         raise RuntimeError("end-to-end result differs from the device-resident step's")
     e2e_ms = allreduce_max(e0.elapsed_time(e1), ws, dev)
-    e2e_value = aggregate_tflops(FLOPS_PER_STEP, args.steps, e2e_ms, ws)
+    e2e_value = aggregate_tflops(FLOPS_PER_STEP * args.steps, e2e_ms, ws, dev)
     h2d = (w.numel() + x.numel()) * 2
     d2h = (y.numel() + ys.numel()) * 2
 
@@ -442,7 +513,11 @@ def run_ours(args):
     clocks = sampler.summary()
     traffic = profiled_traffic("ts_kernel")
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "value_definition": ("composite: the linear FLOPs of a step (nf4_linear at M = 2048 and at M = 16) over "
+                             "the time of the whole step, which also quantizes and dequantizes the weight; the "
+                             "per-kernel figures are under 'kernels' and 'configs'"),
+        "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(args),
@@ -468,6 +543,7 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }
+    line["configs"] = configs_block(dev)
     if not args.no_geglu:
         line["geglu"] = geglu_block(dev)
     if not args.no_dtypes:
@@ -478,6 +554,83 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))
     return 0
+
+
+def _timed_median(fn, stream, reps: int, flush):
+    """Median CUDA-event time (ms) of `fn` over `reps` calls, L2 flushed
+    before each (a memset larger than L2, then a read, so the lines are clean)."""
+    import torch
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush[0].zero_()
+        flush[1].max()
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def configs_block(dev, reps: int = 20):
+    """Each workload's own figures: nf4_quantize and nf4_dequantize of its
+    weight (GB/s of 2.5625 B per weight against the HBM peak) and nf4_linear
+    at its batch -- TFLOP/s against the bf16 peak for M >= 128, GB/s of the
+    algorithmic bytes (0.5625 B per weight + X + Y) against the HBM peak for
+    the skinny batches.  Median of `reps` calls, L2 flushed before each."""
+    import torch
+    import nf4_weight_quantized_quantize_gb300 as nf4
+
+    stream = torch.cuda.current_stream(dev)
+    flush = (torch.empty(512 << 20, dtype=torch.uint8, device=dev),
+             torch.zeros(256 << 20, dtype=torch.uint8, device=dev))
+    pk, pk_kind = peaks()
+    out = {"timing": f"median of {reps} calls, CUDA events, L2 flushed before each (512 MiB memset + 256 MiB read)",
+           "peaks": f"{pk_kind}: HBM {pk['hbm_gbs']} GB/s, bf16 {pk['bf16_tflops']} TFLOP/s"}
+    cases = [(workloads.TINY, (workloads.TINY.m,)), (workloads.Q_PROJ, (workloads.Q_PROJ.m, SKINNY_M)),
+             (workloads.GATE_UP, (workloads.GATE_UP.m, SKINNY_M)), (workloads.DOWN, (workloads.DOWN.m, SKINNY_M))]
+    for cfg, batches in cases:
+        w = workloads.make_weight(cfg, device=dev)
+        numel = w.numel()
+        p = torch.empty(numel // 2, dtype=torch.uint8, device=dev)
+        a = torch.empty(numel // 64, dtype=torch.float32, device=dev)
+        wd = torch.empty(numel, dtype=torch.bfloat16, device=dev)
+        t_q = _timed_median(lambda: nf4.quantize(w, out=(p, a)), stream, reps, flush)
+        t_d = _timed_median(lambda: nf4.dequantize(p, a, numel, out=wd), stream, reps, flush)
+        del w, wd
+        q_gbs = numel * BYTES_PER_W_QUANT / (t_q * 1e-3) / 1e9
+        d_gbs = numel * BYTES_PER_W_DEQUANT / (t_d * 1e-3) / 1e9
+        ent = {"N": cfg.n, "K": cfg.k,
+               "nf4_quantize": {"ms": t_q, "GB/s": q_gbs, "frac_hbm": q_gbs / pk["hbm_gbs"]},
+               "nf4_dequantize": {"ms": t_d, "GB/s": d_gbs, "frac_hbm": d_gbs / pk["hbm_gbs"]}}
+        x_all = workloads.make_activation(cfg, device=dev)
+        for m in batches:
+            x = x_all[:m].contiguous()
+            y = torch.empty(m, cfg.n, dtype=torch.bfloat16, device=dev)
+            _, wsb = nf4.nf4_linear_workspace_size(m, cfg.n, cfg.k)
+            wsp = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+            t = _timed_median(lambda: nf4.linear(x, p, a, cfg.n, out=y, workspace=wsp), stream, reps, flush)
+            tf = 2 * m * cfg.n * cfg.k / (t * 1e-3) / 1e12
+            byts = numel * 0.5625 + 2 * m * cfg.k + 2 * m * cfg.n
+            gbs = byts / (t * 1e-3) / 1e9
+            e = {"ms": t, "TFLOP/s": tf, "GB/s": gbs, "bytes": byts}
+            if m >= 128:
+                e["frac_bf16"] = tf / pk["bf16_tflops"]
+            else:
+                e["frac_hbm"] = gbs / pk["hbm_gbs"]
+            ent[f"nf4_linear_m{m}"] = e
+            del x, y, wsp
+        out[cfg.name.replace(f"_m{cfg.m}", "")] = ent
+        del x_all, p, a
+        torch.cuda.empty_cache()
+    if nf4.nf4_last_error(stream.cuda_stream) != nf4.NF4_OK:
+        raise RuntimeError("a kernel reported a timeout in the per-workload measurement")
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def geglu_block(dev, reps: int = 20):
@@ -501,7 +654,7 @@ def geglu_block(dev, reps: int = 20):
     y2 = torch.empty(cfg.m, 2 * F, dtype=torch.bfloat16, device=dev)
     y1 = torch.empty(cfg.m, F, dtype=torch.bfloat16, device=dev)
     _, wsb = nf4.nf4_linear_workspace_size(SKINNY_M, 2 * F, cfg.k)
-    wsp = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    wsp = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     def timed(fn):

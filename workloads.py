@@ -14,7 +14,7 @@ bf16.  No trained weights are involved.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, replace
 
 import torch
 
@@ -63,6 +63,12 @@ def stack_layer(layer: int, proj_idx: int, m: int = STACK_M) -> Linear:
     name, n, k = PROJECTIONS[proj_idx]
     return Linear(f"gemma3_12b_l{layer}_{name}_m{m}", m, n, k,
                   w_seed=10000 + 10 * layer + proj_idx, x_seed=20000 + 10 * layer + proj_idx)
+
+
+def for_replica(cfg: Linear, rank: int) -> Linear:
+    """The workload as replica `rank` of a batch-parallel run draws it: the same
+    weight (one model, replicated) and its own prompts (X seed + 1000 rank)."""
+    return replace(cfg, name=f"{cfg.name}_rank{rank}" if rank else cfg.name, x_seed=cfg.x_seed + 1000 * rank)
 
 
 def _gen(seed: int, device) -> torch.Generator:
