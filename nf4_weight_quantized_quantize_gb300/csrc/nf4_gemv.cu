@@ -274,9 +274,6 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int nst = (nkb + BL - 1) / BL;
     const int n0 = tile * (PAIR ? C::R / 2 : C::R);   // first weight row (gate row of a pair)
 
-    // byte table: entry b of lane l at word 64 b + l
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem);
-    for (int e = threadIdx.x; e < 256 * 32; e += kGvThreads) lut[64 * (e >> 5) + (e & 31)] = lut_entry<DT>(e >> 5);
     if (threadIdx.x == 0) {
         for (int p = 0; p < SP; ++p) {
             // the expect-tx arrive (+ one cp.async arrive per producer lane when
@@ -296,6 +293,16 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     __syncthreads();
     pdl_wait();   // the previous kernel on the stream has finished
     pdl_launch_dependents();
+    // the producer starts loading at once; the consumers build the byte table
+    // meanwhile (entry b of lane l at word 64 b + l: consumer thread c writes
+    // the 16 copies of lanes 16 (c % 2) .. 16 (c % 2) + 15 of byte c / 2)
+    if (warp < kGvWarps) {
+        const uint32_t e = lut_entry<DT>(threadIdx.x >> 1);
+        uint4* dst = reinterpret_cast<uint4*>(smem + 256 * (threadIdx.x >> 1) + 64 * (threadIdx.x & 1));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(e, e, e, e);
+        consumers_sync();
+    }
 
     if (warp == kGvWarps) {
         // ---------------- producer: stage i into ring slot i % SP once every
@@ -500,35 +507,45 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
             *reinterpret_cast<float4*>(part(split) + nt * 128) = make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
-        __threadfence();
     }
+    // The barrier orders every consumer's partial before thread 0's arrival,
+    // whose acquire-release atomic publishes them (cumulatively) to the CTA
+    // that arrives last and acquires the others' partials for it.
     consumers_sync();
     if (threadIdx.x == 0) {
-        const uint32_t before = atomicAdd(a.counters + tile, 1u);
+        uint32_t before;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(a.counters + tile) : "memory");
         const bool last = before == static_cast<uint32_t>(a.splits - 1);
-        if (last) atomicExch(a.counters + tile, 0u);   // ready for the next call
+        if (last) a.counters[tile] = 0u;   // ready for the next call: nothing else touches it in this one
         *last_flag = last ? 1 : 0;
     }
     consumers_sync();
     if (!*last_flag || !owner) return;
-    __threadfence();
+    // all partials of the tile, summed in split order; loads issued 8 splits at a time
     float sum[NT][4];
+    for (int s0 = 0; s0 < a.splits; s0 += 8) {
+        float4 w4[8][NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+        for (int i = 0; i < 8; ++i) {
+            const int s = s0 + i;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sum[nt][q] = 0.0f;
-    for (int s = 0; s < a.splits; ++s) {
+            for (int nt = 0; nt < NT; ++nt) {
+                if (s == split)
+                    w4[i][nt] = make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
+                else if (s < a.splits)
+                    w4[i][nt] = ldg_cg_f4(part(s) + nt * 128);
+            }
+        }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float4 w4;
-            if (s == split)
-                w4 = make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
-            else
-                w4 = ldg_cg_f4(part(s) + nt * 128);
-            if (s == 0) {
-                sum[nt][0] = w4.x; sum[nt][1] = w4.y; sum[nt][2] = w4.z; sum[nt][3] = w4.w;
-            } else {
-                sum[nt][0] += w4.x; sum[nt][1] += w4.y; sum[nt][2] += w4.z; sum[nt][3] += w4.w;
+        for (int i = 0; i < 8; ++i) {
+            if (s0 + i >= a.splits) break;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (s0 + i == 0) {
+                    sum[nt][0] = w4[i][nt].x; sum[nt][1] = w4[i][nt].y; sum[nt][2] = w4[i][nt].z; sum[nt][3] = w4[i][nt].w;
+                } else {
+                    sum[nt][0] += w4[i][nt].x; sum[nt][1] += w4[i][nt].y; sum[nt][2] += w4[i][nt].z; sum[nt][3] += w4[i][nt].w;
+                }
             }
         }
     }
