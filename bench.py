@@ -69,7 +69,8 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# what the roofline kernel (wide_kernel: nf4_linear at M = 2048) is built from
+# what the roofline kernel (wide_kernel, the CTA-pair GEMM nf4_linear runs at
+# M = 2048 on this shape) is built from
 GEMM_SOURCES = ("nf4_device.cuh", "nf4_convert.cuh", "nf4_gemm_wide.cu", "nf4_launch.h")
 ROOFLINE_KERNEL = "wide_kernel"
 

@@ -78,6 +78,20 @@ __device__ __forceinline__ void expand8_lut(uint32_t p, const uint32_t* lut_lane
     o[3] = mul2<DT>(lut_lane[32u * prmt(p, 0u, 0x4443u)], am2);
 }
 
+// Whether a converter warp of a tcgen05 kernel reports stage st as
+// converted.  Always true in the library.  A test build (-DNF4_TEST_DROP_CONVERTED_ARRIVE) withholds the
+// report for stage 0 -- a flag that nothing sets -- so the MMA issuer's bounded
+// wait runs out and the timeout path (error word, drain, TMEM release, early
+// exit) can be checked on a GPU without faulting or hanging it.
+__device__ __forceinline__ bool report_converted(int st) {
+#ifdef NF4_TEST_DROP_CONVERTED_ARRIVE
+    return st != 0;
+#else
+    (void)st;
+    return true;
+#endif
+}
+
 // Wait (bounded) for the copies a producer issued into the last `slots`
 // stages of its ring to land, so no TMA or cp.async write targets shared
 // memory after exit.

@@ -102,20 +102,6 @@ __device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arri
     mbar_init(bar.drain(1), 1);
 }
 
-// Whether a converter warp reports stage st as converted.  Always true in
-// the library.  A test build (-DNF4_TEST_DROP_CONVERTED_ARRIVE) withholds the
-// report for stage 0 -- a flag that nothing sets -- so the MMA issuer's bounded
-// wait runs out and the timeout path (error word, drain, TMEM release, early
-// exit) can be checked on a GPU without faulting or hanging it.
-__device__ __forceinline__ bool report_converted(int st) {
-#ifdef NF4_TEST_DROP_CONVERTED_ARRIVE
-    return st != 0;
-#else
-    (void)st;
-    return true;
-#endif
-}
-
 // Error-path exit of an MMA issuer: wait (bounded) until every MMA it issued
 // has completed, so TMEM can be released.
 __device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint32_t* err) {

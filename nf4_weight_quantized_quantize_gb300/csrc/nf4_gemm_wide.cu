@@ -1,37 +1,42 @@
-// nf4_gemm_wide.cu -- the fused NF4 GEMM for larger batches (M > 256):
+// nf4_gemm_wide.cu -- the fused NF4 GEMM for larger batches on CTA pairs:
 // Y[M, N] = X[M, K] . deq(W)[N, K]^T at bf16 or fp16, fp32 accumulation in
-// TMEM, tcgen05 kind::f16.
+// TMEM, tcgen05 kind::f16 with cta_group::2 (one MMA spans the tensor cores
+// of the two SMs of a CTA pair).
 //
 // This is the forward of the NF4 linear module of the diffuseR page "Gemma3
 // NF4 on GPU" (#39, Summary: ltx23_nf4_linear) for the prompt batches of the
 // text encoder.  Like the tile kernel (nf4_gemm.cu) it runs swap-AB -- the
-// expanded weight tile is operand A (128 weight rows), the activations are
-// operand B, the accumulator holds Y^T -- but the expanded weights go to
-// shared memory instead of tensor memory.  That frees all 512 TMEM columns
-// for two accumulators of up to 256 activation rows each, so every expanded
-// 128 x 64 weight slab feeds up to 512 activation rows: half the expansion
-// work per FLOP of the tile kernel, whose converter warps, not the tensor
-// pipe, set its pace.
+// expanded weights are operand A, the activations operand B, the accumulator
+// holds Y^T -- with two differences:
+//   - the expanded weights go to shared memory (the K-major 128-byte-swizzle
+//     layout the MMA descriptor reads), so all 512 TMEM columns hold two
+//     accumulators of NX (<= 256) activation rows: every expanded 128 x 64
+//     weight slab feeds 2 NX activation rows, half the expansion work per FLOP
+//     of the tile kernel, whose converter warps set its pace;
+//   - a pair of CTAs shares each MMA (M = 256): each CTA expands its own 128
+//     weight rows and loads only its half of each accumulator's activation
+//     rows, and each SM's tensor core reads the other half from the peer CTA's
+//     shared memory.  A K-slice then costs each CTA 32 KB of activations
+//     instead of 64, and its 4-slot activation ring spans 4 K-slices (a single
+//     CTA this wide cannot hide the activation tiles' load latency within its
+//     shared memory: its MMA issuer waited on them about a quarter of the time).
+// The pair's tile is 256 weight rows x 2 NX activation rows over the whole K.
 //
-// Per CTA: a tile of 128 weight rows x 2 NX activation rows over the whole K.
-// Three rings:
-//   activations: SX slots of one half K-slice (32 values = 64 bytes of each
-//     of the 2 NX rows; two TMA boxes of NX rows, 64-byte swizzle), each
-//     released by its own MMA commit, so loads run up to SX - 1 half-slices
-//     ahead of the tensor core;
-//   expanded weights: SA slots of two K-slices, 128 rows x 128 bytes each in
-//     the K-major 128-byte-swizzle layout the MMA descriptor reads (16-byte
-//     chunk c of row r at chunk c ^ (r % 8)), written by the converter warps
-//     with st.shared and released by a commit after the stage's MMAs;
-//   packed weights: SP slots of two K-slices of packed bytes and fp32 scales
-//     (the tile kernel's weight producer).
-// Warps: 0 loads activations (TMA, lane 0); 1 allocates TMEM and its lane 0
-// issues the MMAs; 2-17 are converters (one thread per weight row and half
-// K-slice: 16 packed bytes expanded through register byte permutes, scaled
-// by the block absmax exactly as the dequantizer does), then the epilogue;
-// 18 loads the packed weights.  Every wait is bounded (NF4_WAIT_LIMIT_NS);
-// on expiry the CTA records an error code, drains what it has in flight,
-// frees TMEM and returns.
+// Rings (per CTA): activations, SX slots of one K-slice (NX rows x 128 bytes:
+// the CTA's halves of both accumulators, TMA with the 128-byte swizzle);
+// expanded weights, SA slots of one K-slice written by the converters;
+// packed weights, SP slots of two K-slices of packed bytes and fp32 scales.
+// Warps: 0 loads activations (both CTAs' copies complete on the even CTA's
+// barrier); 1 allocates TMEM (both CTAs) and in the even CTA issues the
+// MMAs; 2-17 are converters, then the epilogue; 18 loads packed weights.  In
+// the odd CTA, warps 19 and 1 pass each "K-slice expanded" (even and odd
+// K-slices) on to the even CTA.  MMA completion is
+// committed to the barriers of both CTAs.  Every wait is bounded
+// (NF4_WAIT_LIMIT_NS); on expiry the CTA records an error code, drains what it
+// has in flight and frees TMEM, and the peer's waits on it expire in turn.
+// The odd CTA cannot observe its activation copies (they complete on the even
+// CTA's barrier), so on that path it waits a fixed 1 ms -- orders of magnitude
+// above a copy's latency -- before the pair's closing cluster barrier.
 #include <algorithm>
 #include <cmath>
 
@@ -46,34 +51,36 @@ namespace nf4 {
 namespace {
 
 constexpr int kWdKs = 2;                               // K-slices per stage
-constexpr int kWdRs = 2;                               // converter threads per weight row and K-slice
-constexpr int kWdConvWarps = 4 * kWdKs * kWdRs;        // 16
+constexpr int kWdConvWarps = 16;                       // 4 lane quarters x 2 K-slices x 2 halves
 constexpr int kWdWprodWarp = 2 + kWdConvWarps;         // 18
-constexpr int kWdThreads = 32 * (kWdWprodWarp + 1);    // 608
+constexpr int kWdRelayWarp = kWdWprodWarp + 1;         // 19
+constexpr int kWdThreads = 32 * (kWdRelayWarp + 1);    // 640
+constexpr uint64_t kWdSettleNs = 1000000;              // error path: time for copies in flight to land
 constexpr int kWdSmemLimit = 232448;
 constexpr int kWdAccStride = 256;                      // TMEM columns between the two accumulators
 
 template <int NX>
 struct WdCfg {
-    static constexpr int BW = 128;                             // weight rows per tile
-    static constexpr int XH = 2 * NX * 64;                     // activation half-slice slot
+    static constexpr int BW = 128;                             // weight rows per CTA
+    static constexpr int XS = NX * 128;                        // activation slot: NX rows (2 halves of NX / 2)
     static constexpr int A_KS = BW * 128;                      // one expanded K-slice (16 KB)
-    static constexpr int A_SLOT = kWdKs * A_KS;
     static constexpr int P_BYTES = BW * kPackedRow * kWdKs;    // packed bytes of a stage
     static constexpr int AM_BYTES = BW * 4 * kWdKs;            // scales of a stage
     static constexpr int P_SLOT = (P_BYTES + AM_BYTES + 1023) / 1024 * 1024;
-    static constexpr int SA = 2;
+    static constexpr int SA = 4;                               // expanded-weight slots, one K-slice each
     static constexpr int SP = 3;
     static constexpr int BUDGET = kWdSmemLimit - 1024 - 512;   // alignment slack; barriers and flags
-    static constexpr int SX_FIT = (BUDGET - SA * A_SLOT - SP * P_SLOT) / XH;
+    static constexpr int SX_FIT = (BUDGET - SA * A_KS - SP * P_SLOT) / XS;
     static constexpr int SX = SX_FIT > 8 ? 8 : SX_FIT;
-    static constexpr int OFF_A = SX * XH;
-    static constexpr int OFF_P = OFF_A + SA * A_SLOT;
+    static constexpr int OFF_A = SX * XS;
+    static constexpr int OFF_P = OFF_A + SA * A_KS;
     static constexpr int OFF_BAR = OFF_P + SP * P_SLOT;
-    static constexpr int NBAR = 2 * SX + 2 * SA + 2 * SP + 2;   // + accum, drain
+    // xfull, xempty (SX each); afull, aempty, peer_a (SA each); pfull,
+    // pempty (SP each); accum, drain
+    static constexpr int NBAR = 2 * SX + 3 * SA + 2 * SP + 2;
     static constexpr size_t SMEM = 1024 + OFF_BAR + 8 * NBAR + 16;
-    static_assert(NX % 16 == 0 && NX >= 16 && NX <= 256, "MMA N");
-    static_assert(XH % 1024 == 0, "slot alignment");
+    static_assert(NX % 32 == 0 && NX >= 32 && NX <= 256, "MMA N, two halves of a multiple of 16");
+    static_assert(XS % 1024 == 0, "slot alignment");
     static_assert(SX >= 3, "activation ring depth");
     static_assert(SMEM <= kWdSmemLimit, "shared memory budget");
     // packed tile: rows of 64 bytes loaded with the 64-byte swizzle (16-byte
@@ -93,22 +100,119 @@ struct WdArgs {
     uint32_t* err;
 };
 
-// Shared-memory descriptor of a K-major operand in the 64-byte swizzle: rows
-// of 64 bytes, 8-row groups 512 bytes apart (fields as for the 128-byte
-// form: start >> 4, leading offset 1 (unused), stride 512 >> 4, the fixed
-// 0b001 at bits 46-48, swizzle mode 4 = 64 bytes at bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1u) << 16;
-    d |= static_cast<uint64_t>(512u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(4u) << 61;
-    return d;
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive (release, cluster scope) on the barrier at the same shared-memory
+// offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t local_bar, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_bar), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// 2D TMA load into this CTA's shared memory whose completion (complete_tx)
+// is signalled on the barrier at offset `bar` of the even CTA of the pair: the
+// CTA-pair form of the copy, which may signal a barrier of the peer CTA.
+__device__ __forceinline__ void tma_load_2d_pair_leader(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                        int32_t x, int32_t y) {
+    uint32_t leader_bar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(leader_bar) : "r"(bar));
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(leader_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer();
+#pragma unroll 1
+    while (globaltimer() - t0 < ns) {
+    }
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for a barrier the peer CTA arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint32_t* err, volatile int* abort,
+                                                  uint32_t code) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+#pragma unroll 1
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > NF4_WAIT_LIMIT_NS) {
+            record_error(err, code);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---- tcgen05 in CTA-pair form (a kernel uses one form throughout)
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A . B^T over the pair: A's rows split between the two CTAs (128
+// each, at the same shared-memory offset), B's columns likewise, D of each
+// SM in its own TMEM at the same address.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at this offset in both CTAs of the pair when
+// every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
 }
 
 template <int NX, int DT>
@@ -117,6 +221,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     using C = WdCfg<NX>;
     static_assert(DT == kBF16 || DT == kF16, "kind::f16 operand types");
     constexpr int SX = C::SX, SA = C::SA, SP = C::SP;
+    constexpr int HX = NX / 2;   // activation rows of one accumulator held by each CTA
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KB aligned
     uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -127,19 +232,21 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     auto xempty = [&](int i) { return b0 + 8u * (SX + i); };
     auto afull = [&](int i) { return b0 + 8u * (2 * SX + i); };
     auto aempty = [&](int i) { return b0 + 8u * (2 * SX + SA + i); };
-    auto pfull = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + i); };
-    auto pempty = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + SP + i); };
-    const uint32_t accum = b0 + 8u * (2 * SX + 2 * SA + 2 * SP);
+    auto peer_a = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + i); };
+    auto pfull = [&](int i) { return b0 + 8u * (2 * SX + 3 * SA + i); };
+    auto pempty = [&](int i) { return b0 + 8u * (2 * SX + 3 * SA + SP + i); };
+    const uint32_t accum = b0 + 8u * (2 * SX + 3 * SA + 2 * SP);
     const uint32_t drain = accum + 8u;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // tiles run m-fastest: CTAs resident together share each weight tile through L2
-    const int m0 = static_cast<int>(blockIdx.x % args.m_tiles) * (2 * NX);
-    const int n0 = static_cast<int>(blockIdx.x / args.m_tiles) * C::BW;
+    const uint32_t rank = cluster_rank();   // 0: issues the pair's MMAs
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    // pairs run m-fastest: pairs resident together share each weight tile through L2
+    const int m0 = (pair % args.m_tiles) * (2 * NX);
+    const int n0 = (pair / args.m_tiles) * (2 * C::BW) + static_cast<int>(rank) * C::BW;   // this CTA's weight rows
     const int nk = args.K / kBK;
     const int nst = (nk + kWdKs - 1) / kWdKs;
-    const int nhalf = 2 * nk;   // activation half-slices
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SX; ++i) {
@@ -147,8 +254,9 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             mbar_init(xempty(i), 1);
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(afull(i), kWdConvWarps);
+            mbar_init(afull(i), kWdConvWarps / kWdKs);   // the warps that expand one K-slice
             mbar_init(aempty(i), 1);
+            mbar_init(peer_a(i), 1);
         }
         for (int i = 0; i < SP; ++i) {
             mbar_init(pfull(i), kPfullArrivals);
@@ -164,34 +272,63 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         tma_prefetch_desc(&tm_w);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();   // the previous kernel on the stream has finished
     pdl_launch_dependents();
 
+    // ---------------- relay (odd CTA): pass each "K-slice expanded" of the
+    // K-slices h, h + 2, ... on to the even CTA's peer_a barrier -- one
+    // cluster-scope arrival per K-slice instead of one per converter warp, from
+    // two threads in different warps, as each such arrival takes the better part
+    // of a K-slice's MMA time
+    auto relay = [&](int h) {
+        for (int k = h; k < nk; k += kWdKs) {
+            const int a = k % SA;
+            if (!mbar_wait(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted)) break;
+            mbar_arrive_remote(peer_a(a), 0);
+        }
+    };
+
     if (warp == 0) {
-        // ---------------- activation producer: half-slice q into slot q % SX
-        // once the MMAs that read its previous contents completed
+        // ---------------- activation producer: K-slice k into slot k % SX once
+        // the pair's MMAs that read its previous contents completed.  Both
+        // CTAs' copies complete on the even CTA's xfull barrier, which the even
+        // CTA arms with the pair's bytes (the odd CTA's may land first: the
+        // barrier's transaction count goes below zero until it is armed).
         if (lane == 0) {
             int issued = 0;
-            for (int q = 0; q < nhalf; ++q) {
-                const int x = q % SX;
-                if (q >= SX &&
-                    !mbar_wait(xempty(x), ((q / SX) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty))
+            for (int k = 0; k < nk; ++k) {
+                const int x = k % SX;
+                if (k >= SX &&
+                    !mbar_wait_cluster(xempty(x), ((k / SX) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty))
                     break;
                 if (*abort_flag) break;
-                const uint32_t dst = smem_u32(smem + x * C::XH);
-                mbar_arrive_expect_tx(xfull(x), C::XH);
-                tma_load_2d(dst, &tm_x, xfull(x), q * 32, m0);
-                tma_load_2d(dst + NX * 64, &tm_x, xfull(x), q * 32, m0 + NX);
+                const uint32_t dst = smem_u32(smem + x * C::XS);
+                // this CTA's halves of the two accumulators' activation rows
+                const int r0 = m0 + static_cast<int>(rank) * HX;
+                if (rank == 0) {
+                    mbar_arrive_expect_tx(xfull(x), 2 * C::XS);
+                    tma_load_2d(dst, &tm_x, xfull(x), k * kBK, r0);
+                    tma_load_2d(dst + HX * 128, &tm_x, xfull(x), k * kBK, r0 + NX);
+                } else {
+                    tma_load_2d_pair_leader(dst, &tm_x, xfull(x), k * kBK, r0);
+                    tma_load_2d_pair_leader(dst + HX * 128, &tm_x, xfull(x), k * kBK, r0 + NX);
+                }
                 ++issued;
             }
-            if (*abort_flag) drain_ring(xfull(0), SX, issued, args.err);
+            if (*abort_flag) {
+                if (rank == 0)
+                    drain_ring(xfull(0), SX, issued, args.err);
+                else   // its copies complete on the even CTA's barriers: give them time to land
+                    spin_ns(kWdSettleNs);
+            }
         }
     } else if (warp == kWdWprodWarp) {
         // ---------------- weight producer: stage st's packed bytes and scales
@@ -211,53 +348,49 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
         if (*abort_flag && lane == 0) drain_ring(pfull(0), SP, issued, args.err);
     } else if (warp == 1) {
-        // ---------------- MMA issuer: per stage, wait for the expanded weights;
-        // per activation half-slice, wait for it, 2 k-steps x 2 accumulators,
-        // one commit that releases the half-slice; one commit per stage that
-        // releases the weight slot
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16kind_f32<DT>(128, NX);
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer of the pair: per K-slice, wait until
+            // both CTAs expanded its weights and both CTAs' activation halves
+            // landed; 4 k-steps x 2 accumulators; commits to both CTAs that
+            // release the K-slice's activation and expanded-weight slots
+            constexpr uint32_t idesc = idesc_f16kind_f32<DT>(256, NX);
             const uint32_t a_base = smem_u32(smem + C::OFF_A);
             const uint32_t x_base = smem_u32(smem);
             bool ok = true;
-            for (int st = 0; st < nst && ok; ++st) {
-                const int a = st % SA;
-                ok = mbar_wait(afull(a), (st / SA) & 1, args.err, abort_flag, kErrTimeoutConverted);
+            for (int k = 0; k < nk; ++k) {
+                const int a = k % SA;
+                const int x = k % SX;
+                ok = mbar_wait(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
+                     mbar_wait_cluster(peer_a(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
+                     mbar_wait_cluster(xfull(x), (k / SX) & 1, args.err, abort_flag, kErrTimeoutFull);
                 if (!ok) break;
-                const int kbs = min(kWdKs, nk - st * kWdKs);
-                for (int h = 0; h < kbs && ok; ++h) {
+                tc_fence_after();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int q = 2 * (st * kWdKs + h) + half;
-                        const int x = q % SX;
-                        ok = mbar_wait(xfull(x), (q / SX) & 1, args.err, abort_flag, kErrTimeoutFull);
-                        if (!ok) break;
-                        tc_fence_after();
+                for (int j = 0; j < 4; ++j) {
+                    // k-step j of the K-slice: 32 bytes of each row
+                    const uint64_t adesc = smem_desc_sw128(a_base + a * C::A_KS + 32 * j);
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            // k-step 2 half + j of the K-slice: 32 bytes of each row
-                            const uint64_t adesc =
-                                smem_desc_sw128(a_base + a * C::A_SLOT + h * C::A_KS + 32 * (2 * half + j));
-#pragma unroll
-                            for (int acc = 0; acc < 2; ++acc) {
-                                const uint64_t bdesc = smem_desc_sw64(x_base + x * C::XH + acc * NX * 64 + 32 * j);
-                                const uint32_t first = (st == 0 && h == 0 && half == 0 && j == 0) ? 0u : 1u;
-                                mma_bf16(tmem + acc * kWdAccStride, adesc, bdesc, idesc, first);
-                            }
-                        }
-                        mma_commit(xempty(x));
+                    for (int acc = 0; acc < 2; ++acc) {
+                        const uint64_t bdesc = smem_desc_sw128(x_base + x * C::XS + acc * HX * 128 + 32 * j);
+                        const uint32_t first = (k == 0 && j == 0) ? 0u : 1u;
+                        mma_pair(tmem + acc * kWdAccStride, adesc, bdesc, idesc, first);
                     }
                 }
-                if (ok) mma_commit(aempty(a));
+                mma_commit_pair(xempty(x));
+                mma_commit_pair(aempty(a));
             }
             if (ok) {
-                mma_commit(accum);
+                mma_commit_pair(accum);
             } else {
                 int dummy = 0;
-                mma_commit(drain);
+                mma_commit_pair(drain);
                 mbar_wait(drain, 0, args.err, &dummy, kErrTimeoutDrain);
             }
+        } else if (lane == 0) {
+            relay(1);
         }
+    } else if (warp == kWdRelayWarp) {
+        if (lane == 0 && rank == 1) relay(0);
     } else {
         // ---------------- converters: unit u = (warp - 2) / 4 expands half
         // `part` of K-slice h of each stage for weight rows 32 q .. 32 q + 31
@@ -266,20 +399,20 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int h = u % kWdKs;
         const int part = u / kWdKs;
         const int q = warp & 3;
-        const int r = q * 32 + lane;   // weight row within the tile
+        const int r = q * 32 + lane;   // weight row within this CTA's 128
         const CodebookRegs cb = codebook_regs<DT>();
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         bool ok = true;
         for (int st = 0; st < nst; ++st) {
             const int p = st % SP;
-            const int a = st % SA;
+            const int k = st * kWdKs + h;
             const bool got = mbar_wait(pfull(p), (st / SP) & 1, args.err, abort_flag, kErrTimeoutFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             const uint8_t* ptile = smem + C::OFF_P + p * C::P_SLOT;
-            const bool live = st * kWdKs + h < nk;   // warp-uniform: the K-slice exists
+            const bool live = k < nk;   // warp-uniform: the K-slice exists
             uint4 w4 = make_uint4(0, 0, 0, 0);
             float am = 0.0f;
             if (live) {
@@ -288,14 +421,16 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(pempty(p));   // this warp is done with packed slot p
-            // the expanded slot must be free: the MMAs of stage st - SA completed
-            const bool free_slot = st < SA || mbar_wait(aempty(a), ((st / SA) - 1) & 1, args.err, abort_flag,
-                                                        kErrTimeoutEmpty);
+            if (!live) continue;                      // the last stage of an odd number of K-slices
+            // the expanded slot must be free: the pair's MMAs of K-slice k - SA completed
+            const int a = k % SA;
+            const bool free_slot = k < SA || mbar_wait_cluster(aempty(a), ((k / SA) - 1) & 1, args.err,
+                                                               abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, free_slot)) {
                 ok = false;
                 break;
             }
-            if (live) {
+            {
                 // An absmax that is a DT value scales in one paired DT multiply
                 // (exact product, one rounding); any other absmax scales each
                 // value in fp32 and rounds once -- the dequantizer's value.
@@ -312,7 +447,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
                 // 32 values = 4 chunks of 16 bytes: chunks 4 part .. 4 part + 3 of
                 // row r, each stored at chunk ^ (r % 8)
-                const uint32_t row = a_base + a * C::A_SLOT + h * C::A_KS + r * 128;
+                const uint32_t row = a_base + a * C::A_KS + r * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     sts128(row + (((4 * part + c) ^ (r & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
@@ -320,14 +455,15 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             fence_proxy_async_smem();   // the MMAs read the slot through the async proxy
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(a));
+            if (lane == 0 && report_converted(st)) mbar_arrive(afull(a));
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
-        ok = __all_sync(0xffffffffu, ok) && mbar_wait(accum, 0, args.err, abort_flag, kErrTimeoutAccum);
+        ok = __all_sync(0xffffffffu, ok) && mbar_wait_cluster(accum, 0, args.err, abort_flag, kErrTimeoutAccum);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             // accumulator acc: TMEM lane = weight row n0 + r, column c = activation
-            // row m0 + acc NX + c; 16-column chunks round-robin over the 4 units
+            // row m0 + acc NX + c (both CTAs' halves); 16-column chunks round-robin
+            // over the 4 units
             const int n = n0 + r;
             const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
             constexpr int CHUNKS = NX / 16;
@@ -351,26 +487,27 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();   // the pair is done with both TMEMs before either frees them
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc_pair(tmem, 512);
     }
 }
 
 // ============================================================ host side
 
 struct WdPlan {
-    int nx;        // activation rows per accumulator (MMA N)
+    int nx;        // activation rows per accumulator (MMA N), split between the pair
     int m_tiles;   // tiles of 2 nx activation rows
-    int n_tiles;   // tiles of 128 weight rows
+    int n_pairs;   // tiles of 256 weight rows
 };
 
 WdPlan make_wd_plan(int64_t M, int64_t N) {
     WdPlan p;
     p.m_tiles = static_cast<int>((M + 511) / 512);
     const int64_t rows = (M + p.m_tiles - 1) / p.m_tiles;   // balanced tiles of at most 512 rows
-    p.nx = static_cast<int>(((rows + 1) / 2 + 15) / 16 * 16);
-    p.n_tiles = static_cast<int>((N + 127) / 128);
+    p.nx = static_cast<int>(((rows + 1) / 2 + 31) / 32 * 32);
+    p.n_pairs = static_cast<int>((N + 255) / 256);
     return p;
 }
 
@@ -384,19 +521,30 @@ cudaError_t launch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int
         return e;
     CUtensorMap tm_x, tm_w;
     const CUtensorMapDataType xdt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // activations: boxes of 32 values (64 bytes, the swizzle span) x NX rows;
-    // packed weights: boxes of two K-slices (64 bytes) x 128 rows
-    if (!make_map(&tm_x, x, xdt, 2, M, K, NX, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+    // activations: boxes of one K-slice (64 values, 128 bytes: the swizzle
+    // span) x NX / 2 rows; packed weights: boxes of two K-slices x 128 rows
+    if (!make_map(&tm_x, x, xdt, 2, M, K, NX / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, C::BW, kPackedRow * kWdKs,
                   CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const int64_t ctas = 2 * static_cast<int64_t>(p.m_tiles) * p.n_pairs;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     WdArgs a{absmax, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.m_tiles, dev.err_word};
-    if (cudaError_t e = launch_pdl(kernel, dim3(static_cast<unsigned>(tiles)), dim3(kWdThreads), C::SMEM, s, tm_x,
-                                   tm_w, a);
-        e != cudaSuccess)
-        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kWdThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tm_x, tm_w, a); e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
@@ -405,13 +553,9 @@ template <int DT>
 cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
     switch (p.nx) {
-        case 144: return launch_wd<144, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
         case 160: return launch_wd<160, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 176: return launch_wd<176, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
         case 192: return launch_wd<192, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 208: return launch_wd<208, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
         case 224: return launch_wd<224, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 240: return launch_wd<240, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
         case 256: return launch_wd<256, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
         default: return cudaErrorInvalidValue;
     }
@@ -419,21 +563,22 @@ cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, i
 
 }  // namespace
 
-// Whether the wide kernel takes this call, by the same shape-only estimate
-// of both kernels' time: waves of one CTA per SM times the time per K-slice
-// of a tile -- about 750 clocks for the tile kernel (128 x 256, bound by its
-// converter warps) and 8 MMAs of N = nx for the wide one (about 127 clocks
-// per N = 256 MMA; 128 x 2 nx, the same expansion work).
+// Whether the pair kernel takes this call, by a shape-only estimate of both
+// kernels' time: waves of one CTA per SM times the time of a K-slice.  Measured
+// on GB300 at M = 2048 (bf16, L2 flushed): about 0.52 us (1000 clocks) per
+// K-slice for the tile kernel's 128 x 256 tile and 0.81 us (1560 clocks) for a
+// pair's 256 x 512 tile at nx = 256 -- its MMAs scale with nx, its converters
+// and signalling do not, so smaller nx is not taken below the tile kernel's.
 bool wide_applies(int dtype, int64_t M, int64_t N) {
     if ((dtype != kBF16 && dtype != kF16) || M <= 256) return false;
     const WdPlan p = make_wd_plan(M, N);
-    if (p.nx < 144 || p.nx > 256) return false;
+    if (p.nx < 160 || p.nx > 256) return false;
     constexpr double kSms = 152.0;
-    const double n_tiles = static_cast<double>(p.n_tiles);
+    const double n_tiles = std::ceil(N / 128.0);
     const double ts_waves = std::ceil(n_tiles * std::ceil(M / 256.0) / kSms);
-    const double wd_waves = std::ceil(n_tiles * p.m_tiles / kSms);
-    const double wd_slice = std::max(750.0, 8.0 * 127.0 * p.nx / 256.0);
-    return wd_waves * wd_slice < ts_waves * 750.0;
+    const double wd_waves = std::ceil(2.0 * p.n_pairs * p.m_tiles / kSms);
+    const double wd_slice = std::max(1000.0, 1560.0 * p.nx / 256.0);
+    return wd_waves * wd_slice < ts_waves * 1000.0;
 }
 
 cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,

@@ -153,7 +153,7 @@ def test_tile_path_larger_shapes(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (1000, 10000, 192),    # ragged M (the second accumulator half past M) and N, an odd block count
+    (1500, 10000, 192),    # ragged M (the last tile's second accumulator half partly past M) and N, odd block count
     (2047, 4100, 320),     # 4 tiles of 512 rows, the last one ragged; a partial weight tile
     (4096, 2048, 128),     # 8 tiles of 512 rows, one stage
 ])

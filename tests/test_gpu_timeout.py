@@ -3,7 +3,8 @@
 A test build of the library (-DNF4_TEST_DROP_CONVERTED_ARRIVE
 -DNF4_TEST_DROP_CONSUMED_ARRIVE, wait limit 50 ms) withholds two reports,
 flags that nothing else sets: in the tcgen05 kernels the "converted" report
-for the first K-slice, so the MMA issuer's wait on it expires; in the
+for the first K-slice, so the MMA issuer's wait on it expires (in the CTA-pair
+kernel, in both CTAs: the odd CTA's relay times out on its own); in the
 warp-MMA kernel (M <= 16) one warp's "consumed" report for the first ring
 slot, so the producer's wait to refill it expires.  The CTA must then record
 the error word, drain its in-flight copies, release what it holds and return.
@@ -49,8 +50,8 @@ def _inputs(m, n, k, seed):
     return x.to(DEV), torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV), workloads.bits(x), p, a
 
 
-@pytest.mark.parametrize("m,n,k", [(256, 512, 1024), (64, 512, 1024), (16, 19456, 1792)],
-                         ids=["tile_kernel", "split_kernel", "warp_mma_kernel"])
+@pytest.mark.parametrize("m,n,k", [(256, 512, 1024), (64, 512, 1024), (16, 19456, 1792), (1500, 10000, 192)],
+                         ids=["tile_kernel", "split_kernel", "warp_mma_kernel", "pair_kernel"])
 def test_bounded_wait_expires_and_reports(faulty_lib, m, n, k):
     # warp_mma_kernel: 152 tiles of 128 rows, no K split, 7 stages per CTA --
     # one more than its 6-slot ring, so the producer must wait for slot 0
