@@ -28,9 +28,8 @@
 // packed weights, SP slots of two K-slices of packed bytes and fp32 scales.
 // Warps: 0 loads activations (both CTAs' copies complete on the even CTA's
 // barrier); 1 allocates TMEM (both CTAs) and in the even CTA issues the
-// MMAs; 2-17 are converters, then the epilogue; 18 loads packed weights.  In
-// the odd CTA, warps 19 and 1 pass each "K-slice expanded" (even and odd
-// K-slices) on to the even CTA.  MMA completion is
+// MMAs; 2-17 are converters (both CTAs' arrive on the even CTA's barrier),
+// then the epilogue; 18 loads packed weights.  MMA completion is
 // committed to the barriers of both CTAs.  Every wait is bounded
 // (NF4_WAIT_LIMIT_NS); on expiry the CTA records an error code, drains what it
 // has in flight and frees TMEM, and the peer's waits on it expire in turn.
@@ -53,8 +52,7 @@ namespace {
 constexpr int kWdKs = 2;                               // K-slices per stage
 constexpr int kWdConvWarps = 16;                       // 4 lane quarters x 2 K-slices x 2 halves
 constexpr int kWdWprodWarp = 2 + kWdConvWarps;         // 18
-constexpr int kWdRelayWarp = kWdWprodWarp + 1;         // 19
-constexpr int kWdThreads = 32 * (kWdRelayWarp + 1);    // 640
+constexpr int kWdThreads = 32 * (kWdWprodWarp + 1);    // 608
 constexpr uint64_t kWdSettleNs = 1000000;              // error path: time for copies in flight to land
 constexpr int kWdSmemLimit = 232448;
 constexpr int kWdAccStride = 256;                      // TMEM columns between the two accumulators
@@ -75,9 +73,9 @@ struct WdCfg {
     static constexpr int OFF_A = SX * XS;
     static constexpr int OFF_P = OFF_A + SA * A_KS;
     static constexpr int OFF_BAR = OFF_P + SP * P_SLOT;
-    // xfull, xempty (SX each); afull, aempty, peer_a (SA each); pfull,
-    // pempty (SP each); accum, drain
-    static constexpr int NBAR = 2 * SX + 3 * SA + 2 * SP + 2;
+    // xfull, xempty (SX each); afull, aempty (SA each); pfull, pempty (SP
+    // each); accum, drain
+    static constexpr int NBAR = 2 * SX + 2 * SA + 2 * SP + 2;
     static constexpr size_t SMEM = 1024 + OFF_BAR + 8 * NBAR + 16;
     static_assert(NX % 32 == 0 && NX >= 32 && NX <= 256, "MMA N, two halves of a multiple of 16");
     static_assert(XS % 1024 == 0, "slot alignment");
@@ -115,12 +113,12 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive (release, cluster scope) on the barrier at the same shared-memory
-// offset in CTA `rank` of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t local_bar, uint32_t rank) {
+// Arrive (release, CTA scope) on the barrier at the same shared-memory offset
+// in CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t local_bar, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_bar), "r"(rank));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 // 2D TMA load into this CTA's shared memory whose completion (complete_tx)
@@ -232,10 +230,9 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     auto xempty = [&](int i) { return b0 + 8u * (SX + i); };
     auto afull = [&](int i) { return b0 + 8u * (2 * SX + i); };
     auto aempty = [&](int i) { return b0 + 8u * (2 * SX + SA + i); };
-    auto peer_a = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + i); };
-    auto pfull = [&](int i) { return b0 + 8u * (2 * SX + 3 * SA + i); };
-    auto pempty = [&](int i) { return b0 + 8u * (2 * SX + 3 * SA + SP + i); };
-    const uint32_t accum = b0 + 8u * (2 * SX + 3 * SA + 2 * SP);
+    auto pfull = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + i); };
+    auto pempty = [&](int i) { return b0 + 8u * (2 * SX + 2 * SA + SP + i); };
+    const uint32_t accum = b0 + 8u * (2 * SX + 2 * SA + 2 * SP);
     const uint32_t drain = accum + 8u;
 
     const int warp = threadIdx.x >> 5;
@@ -254,9 +251,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             mbar_init(xempty(i), 1);
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(afull(i), kWdConvWarps / kWdKs);   // the warps that expand one K-slice
+            mbar_init(afull(i), kWdConvWarps);   // (even CTA) the 8 warps per CTA that expand a K-slice
             mbar_init(aempty(i), 1);
-            mbar_init(peer_a(i), 1);
         }
         for (int i = 0; i < SP; ++i) {
             mbar_init(pfull(i), kPfullArrivals);
@@ -282,19 +278,6 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const uint32_t tmem = *tmem_slot;
     pdl_wait();   // the previous kernel on the stream has finished
     pdl_launch_dependents();
-
-    // ---------------- relay (odd CTA): pass each "K-slice expanded" of the
-    // K-slices h, h + 2, ... on to the even CTA's peer_a barrier -- one
-    // cluster-scope arrival per K-slice instead of one per converter warp, from
-    // two threads in different warps, as each such arrival takes the better part
-    // of a K-slice's MMA time
-    auto relay = [&](int h) {
-        for (int k = h; k < nk; k += kWdKs) {
-            const int a = k % SA;
-            if (!mbar_wait(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted)) break;
-            mbar_arrive_remote(peer_a(a), 0);
-        }
-    };
 
     if (warp == 0) {
         // ---------------- activation producer: K-slice k into slot k % SX once
@@ -360,8 +343,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             for (int k = 0; k < nk; ++k) {
                 const int a = k % SA;
                 const int x = k % SX;
-                ok = mbar_wait(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
-                     mbar_wait_cluster(peer_a(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
+                ok = mbar_wait_cluster(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
                      mbar_wait_cluster(xfull(x), (k / SX) & 1, args.err, abort_flag, kErrTimeoutFull);
                 if (!ok) break;
                 tc_fence_after();
@@ -386,11 +368,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 mma_commit_pair(drain);
                 mbar_wait(drain, 0, args.err, &dummy, kErrTimeoutDrain);
             }
-        } else if (lane == 0) {
-            relay(1);
         }
-    } else if (warp == kWdRelayWarp) {
-        if (lane == 0 && rank == 1) relay(0);
     } else {
         // ---------------- converters: unit u = (warp - 2) / 4 expands half
         // `part` of K-slice h of each stage for weight rows 32 q .. 32 q + 31
@@ -455,7 +433,20 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             fence_proxy_async_smem();   // the MMAs read the slot through the async proxy
             __syncwarp();
-            if (lane == 0 && report_converted(st)) mbar_arrive(afull(a));
+            // Both CTAs' warps arrive on the even CTA's afull.  The odd CTA's
+            // arrival is a CTA-scope release: the MMA that reads this slot runs
+            // on this SM's tensor core through the async proxy, to which the
+            // fence above has already made the stores visible, and it is issued
+            // only after the arrival is observed -- the pattern of the cluster
+            // pipelines in CUTLASS for thread-written operands of CTA-pair
+            // MMAs.  A cluster-scope release costs about 0.7 us per arrival
+            // (measured), most of the converters' lead over the MMAs.
+            if (lane == 0 && report_converted(st)) {
+                if (rank == 0)
+                    mbar_arrive(afull(a));
+                else
+                    mbar_arrive_remote_cta(afull(a), 0);
+            }
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = __all_sync(0xffffffffu, ok) && mbar_wait_cluster(accum, 0, args.err, abort_flag, kErrTimeoutAccum);

@@ -4,7 +4,7 @@ A test build of the library (-DNF4_TEST_DROP_CONVERTED_ARRIVE
 -DNF4_TEST_DROP_CONSUMED_ARRIVE, wait limit 50 ms) withholds two reports,
 flags that nothing else sets: in the tcgen05 kernels the "converted" report
 for the first K-slice, so the MMA issuer's wait on it expires (in the CTA-pair
-kernel, in both CTAs: the odd CTA's relay times out on its own); in the
+kernel the odd CTA's waits for the MMAs then expire on their own); in the
 warp-MMA kernel (M <= 16) one warp's "consumed" report for the first ring
 slot, so the producer's wait to refill it expires.  The CTA must then record
 the error word, drain its in-flight copies, release what it holds and return.
