@@ -560,9 +560,12 @@ def run_ours(args):
     return 0
 
 
-def _timed_median(fn, stream, reps: int, flush):
-    """Median CUDA-event time (ms) of `fn` over `reps` calls, L2 flushed
-    before each (a memset larger than L2, then a read, so the lines are clean)."""
+def _timed_mean(fn, stream, reps: int, flush):
+    """Mean CUDA-event time (ms) of `fn` over `reps` calls, L2 flushed before
+    each (a memset larger than L2, then a read, so the lines are clean).  The
+    mean, not the median: event timestamps on GB300 advance in steps of
+    2.048 us, so the median of a call of a few microseconds is a whole number
+    of steps, while the mean of many calls averages the steps out."""
     import torch
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     fn()
@@ -576,15 +579,15 @@ def _timed_median(fn, stream, reps: int, flush):
         e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
-    return statistics.median(ts)
+    return statistics.mean(ts)
 
 
-def configs_block(dev, reps: int = 20):
+def configs_block(dev, reps: int = 50):
     """Each workload's own figures: nf4_quantize and nf4_dequantize of its
     weight (GB/s of 2.5625 B per weight against the HBM peak) and nf4_linear
     at its batch -- TFLOP/s against the bf16 peak for M >= 128, GB/s of the
     algorithmic bytes (0.5625 B per weight + X + Y) against the HBM peak for
-    the skinny batches.  Median of `reps` calls, L2 flushed before each."""
+    the skinny batches.  Mean of `reps` calls, L2 flushed before each."""
     import torch
     import nf4_weight_quantized_quantize_gb300 as nf4
 
@@ -592,7 +595,8 @@ def configs_block(dev, reps: int = 20):
     flush = (torch.empty(512 << 20, dtype=torch.uint8, device=dev),
              torch.zeros(256 << 20, dtype=torch.uint8, device=dev))
     pk, pk_kind = peaks()
-    out = {"timing": f"median of {reps} calls, CUDA events, L2 flushed before each (512 MiB memset + 256 MiB read)",
+    out = {"timing": f"mean of {reps} calls, CUDA events (2.048 us timestamp steps), L2 flushed before each "
+                     "(512 MiB memset + 256 MiB read)",
            "peaks": f"{pk_kind}: HBM {pk['hbm_gbs']} GB/s, bf16 {pk['bf16_tflops']} TFLOP/s"}
     cases = [(workloads.TINY, (workloads.TINY.m,)), (workloads.Q_PROJ, (workloads.Q_PROJ.m, SKINNY_M)),
              (workloads.GATE_UP, (workloads.GATE_UP.m, SKINNY_M)), (workloads.DOWN, (workloads.DOWN.m, SKINNY_M))]
@@ -602,8 +606,8 @@ def configs_block(dev, reps: int = 20):
         p = torch.empty(numel // 2, dtype=torch.uint8, device=dev)
         a = torch.empty(numel // 64, dtype=torch.float32, device=dev)
         wd = torch.empty(numel, dtype=torch.bfloat16, device=dev)
-        t_q = _timed_median(lambda: nf4.quantize(w, out=(p, a)), stream, reps, flush)
-        t_d = _timed_median(lambda: nf4.dequantize(p, a, numel, out=wd), stream, reps, flush)
+        t_q = _timed_mean(lambda: nf4.quantize(w, out=(p, a)), stream, reps, flush)
+        t_d = _timed_mean(lambda: nf4.dequantize(p, a, numel, out=wd), stream, reps, flush)
         del w, wd
         q_gbs = numel * BYTES_PER_W_QUANT / (t_q * 1e-3) / 1e9
         d_gbs = numel * BYTES_PER_W_DEQUANT / (t_d * 1e-3) / 1e9
@@ -616,7 +620,7 @@ def configs_block(dev, reps: int = 20):
             y = torch.empty(m, cfg.n, dtype=torch.bfloat16, device=dev)
             _, wsb = nf4.nf4_linear_workspace_size(m, cfg.n, cfg.k)
             wsp = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
-            t = _timed_median(lambda: nf4.linear(x, p, a, cfg.n, out=y, workspace=wsp), stream, reps, flush)
+            t = _timed_mean(lambda: nf4.linear(x, p, a, cfg.n, out=y, workspace=wsp), stream, reps, flush)
             tf = 2 * m * cfg.n * cfg.k / (t * 1e-3) / 1e12
             byts = numel * 0.5625 + 2 * m * cfg.k + 2 * m * cfg.n
             gbs = byts / (t * 1e-3) / 1e9
