@@ -437,10 +437,10 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             // arrival is a CTA-scope release: the MMA that reads this slot runs
             // on this SM's tensor core through the async proxy, to which the
             // fence above has already made the stores visible, and it is issued
-            // only after the arrival is observed -- the pattern of the cluster
-            // pipelines in CUTLASS for thread-written operands of CTA-pair
-            // MMAs.  A cluster-scope release costs about 0.7 us per arrival
-            // (measured), most of the converters' lead over the MMAs.
+            // only after the arrival is observed (CUTLASS's cluster barrier
+            // arrives from a peer CTA in the same default CTA-scope form).  A
+            // cluster-scope release costs about 0.7 us per arrival (measured),
+            // most of the converters' lead over the MMAs.
             if (lane == 0 && report_converted(st)) {
                 if (rank == 0)
                     mbar_arrive(afull(a));
