@@ -33,6 +33,7 @@ import ctypes
 import hashlib
 import json
 import os
+import random
 import re
 import statistics
 import sys
@@ -416,6 +417,7 @@ def run_ours(args):
     t_wall = time.perf_counter()
     for k in range(args.steps):
         flush_l2()
+        phase_jitter()
         step_ev[k][0].record(stream)
         step()
         step_ev[k][1].record(stream)
@@ -436,6 +438,7 @@ def run_ours(args):
     call_ev = [[(mk(), mk()) for _ in calls] for _ in range(call_steps)]
     for k in range(call_steps):
         flush_l2()
+        phase_jitter()
         step(call_ev[k])
     torch.cuda.synchronize()
     per_call = [statistics.mean(call_ev[k][i][0].elapsed_time(call_ev[k][i][1]) for k in range(call_steps))
@@ -560,12 +563,27 @@ def run_ours(args):
     return 0
 
 
+_JITTER = random.Random(20261203)
+
+
+def phase_jitter():
+    """Spin the device for a random 0-4095 clocks (0-2 us) before a start
+    event.  CUDA event timestamps on GB300 advance in steps of 2.048 us; with
+    the phase of the start fixed (an L2 flush of constant length before every
+    call) the mean of many short intervals keeps that quantisation, with a
+    random phase it does not."""
+    import torch
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(_JITTER.randrange(0, 4096))
+
+
 def _timed_mean(fn, stream, reps: int, flush):
     """Mean CUDA-event time (ms) of `fn` over `reps` calls, L2 flushed before
-    each (a memset larger than L2, then a read, so the lines are clean).  The
-    mean, not the median: event timestamps on GB300 advance in steps of
-    2.048 us, so the median of a call of a few microseconds is a whole number
-    of steps, while the mean of many calls averages the steps out."""
+    each (a memset larger than L2, then a read, so the lines are clean) and
+    the start phase randomised (phase_jitter).  The mean, not the median:
+    event timestamps on GB300 advance in steps of 2.048 us, so the median of a
+    call of a few microseconds is a whole number of steps, while the mean of
+    many calls with random phases is not."""
     import torch
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     fn()
@@ -573,6 +591,7 @@ def _timed_mean(fn, stream, reps: int, flush):
     for _ in range(reps):
         flush[0].zero_()
         flush[1].max()
+        phase_jitter()
         e0, e1 = mk(), mk()
         e0.record(stream)
         fn()
@@ -582,12 +601,52 @@ def _timed_mean(fn, stream, reps: int, flush):
     return statistics.mean(ts)
 
 
+def _skinny_stream(x, p, a, n, y, wsp, stream, calls: int = 64):
+    """Per-call time (ms) of back-to-back nf4_linear calls at a skinny batch,
+    the way a decode loop issues them: call i reads copy i % c of the weight,
+    with c copies holding more than three times the L2, so no call finds its
+    weight in L2.  The calls are captured once in a CUDA graph and replayed
+    between one pair of CUDA events, so the host's per-call launch work
+    (argument checks, tensor-map encoding) does not pace the device."""
+    import torch
+    import nf4_weight_quantized_quantize_gb300 as nf4
+    l2 = getattr(torch.cuda.get_device_properties(x.device), "L2_cache_size", 128 << 20) or (128 << 20)
+    wbytes = p.numel() + 4 * a.numel()
+    copies = max(2, -(-3 * l2 // wbytes))
+    ps = [p.clone() for _ in range(copies)]
+    am = [a.clone() for _ in range(copies)]
+
+    def run():
+        for i in range(calls):
+            nf4.linear(x, ps[i % copies], am[i % copies], n, out=y, workspace=wsp)
+
+    run()   # first calls on this device set up the library's per-device state
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    graph.replay()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    e0, e1 = mk(), mk()
+    torch.cuda.synchronize()
+    phase_jitter()
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / calls
+    del graph, ps, am
+    return ms, copies, calls
+
+
 def configs_block(dev, reps: int = 50):
     """Each workload's own figures: nf4_quantize and nf4_dequantize of its
     weight (GB/s of 2.5625 B per weight against the HBM peak) and nf4_linear
     at its batch -- TFLOP/s against the bf16 peak for M >= 128, GB/s of the
     algorithmic bytes (0.5625 B per weight + X + Y) against the HBM peak for
-    the skinny batches.  Mean of `reps` calls, L2 flushed before each."""
+    the skinny batches.  Mean of `reps` calls, L2 flushed before each; the
+    skinny batches of the large weights also as a stream of back-to-back
+    calls over distinct weight copies (`_skinny_stream`)."""
     import torch
     import nf4_weight_quantized_quantize_gb300 as nf4
 
@@ -629,6 +688,14 @@ def configs_block(dev, reps: int = 50):
                 e["frac_bf16"] = tf / pk["bf16_tflops"]
             else:
                 e["frac_hbm"] = gbs / pk["hbm_gbs"]
+                if numel * 0.5625 >= 4e6:   # a weight L2 cannot hold three times over in a few copies
+                    ms_s, copies, ncalls = _skinny_stream(x, p, a, cfg.n, y, wsp, stream)
+                    g_s = byts / (ms_s * 1e-3) / 1e9
+                    e["stream"] = {"ms_per_call": ms_s, "GB/s": g_s, "frac_hbm": g_s / pk["hbm_gbs"],
+                                   "weight_copies": copies, "calls": ncalls,
+                                   "how": "back-to-back calls over distinct weight copies (> 3x L2 in all), "
+                                          "replayed as one CUDA graph between one pair of events: the "
+                                          "per-call time of a decode loop"}
             ent[f"nf4_linear_m{m}"] = e
             del x, y, wsp
         out[cfg.name.replace(f"_m{cfg.m}", "")] = ent
@@ -670,6 +737,7 @@ def geglu_block(dev, reps: int = 20):
         ev = [(mk(), mk()) for _ in range(reps)]
         for e0, e1 in ev:
             flush.zero_()
+            phase_jitter()
             e0.record(stream)
             fn()
             e1.record(stream)
@@ -719,6 +787,7 @@ def dtypes_block(dev, reps: int = 20):
         ev = [(mk(), mk()) for _ in range(reps)]
         for e0, e1 in ev:
             flush.zero_()
+            phase_jitter()
             e0.record(stream)
             fn()
             e1.record(stream)

@@ -183,8 +183,8 @@ constexpr int acc_sets() {
 // One block of the stage for the warp's RGW row groups: expand rows lo and hi
 // (8 packed bytes each, the lane's share: wl[j], wh[j]) and run the block's
 // four MMA steps against the activation fragments xl (activation rows 0-7)
-// and xh (rows 8-15).  Steps go round the row groups, so each step's table
-// loads and multiplies are independent of the previous step's MMAs.  EXACT:
+// and xh (rows 8-15).  Each step covers all row groups, so its table loads
+// and multiplies are independent of the previous step's MMAs.  EXACT:
 // every absmax of the block is a DT value (one paired DT multiply); else each
 // value is scaled in fp32 and rounded once.
 template <int DT, int NT, int RGW, bool EXACT>
@@ -207,18 +207,33 @@ __device__ __forceinline__ void stage_mma(float (&acc)[RGW][NT][acc_sets<RGW, NT
         else
             return scale_entry<DT>(e, am);
     };
+    // Per step: every row group's table loads first, then the multiplies, then
+    // the MMAs -- 16 independent loads in flight before the first use (about
+    // 7 % faster on down_proj at M = 16 than one row group after another).
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const uint32_t k = (2 * s) & 3;
+        uint32_t e[RGW][4];   // A fragment registers a0..a3 of each row group
 #pragma unroll
         for (int j = 0; j < RGW; ++j) {
             const uint32_t w0 = s < 2 ? wl[j].x : wl[j].y, w1 = s < 2 ? wh[j].x : wh[j].y;
-            const uint32_t a0 = scale(at(w0, k), sl[j], aml[j]);
-            const uint32_t a2 = scale(at(w0, k + 1), sl[j], aml[j]);
-            const uint32_t a1 = scale(at(w1, k), sh[j], amh[j]);
-            const uint32_t a3 = scale(at(w1, k + 1), sh[j], amh[j]);
-            mma16816<DT>(acc[j][0][s % AS], a0, a1, a2, a3, xl[2 * s], xl[2 * s + 1]);
-            if constexpr (NT == 2) mma16816<DT>(acc[j][1][s % AS], a0, a1, a2, a3, xh[2 * s], xh[2 * s + 1]);
+            e[j][0] = at(w0, k);
+            e[j][2] = at(w0, k + 1);
+            e[j][1] = at(w1, k);
+            e[j][3] = at(w1, k + 1);
+        }
+#pragma unroll
+        for (int j = 0; j < RGW; ++j) {
+            e[j][0] = scale(e[j][0], sl[j], aml[j]);
+            e[j][2] = scale(e[j][2], sl[j], aml[j]);
+            e[j][1] = scale(e[j][1], sh[j], amh[j]);
+            e[j][3] = scale(e[j][3], sh[j], amh[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < RGW; ++j) {
+            mma16816<DT>(acc[j][0][s % AS], e[j][0], e[j][1], e[j][2], e[j][3], xl[2 * s], xl[2 * s + 1]);
+            if constexpr (NT == 2)
+                mma16816<DT>(acc[j][1][s % AS], e[j][0], e[j][1], e[j][2], e[j][3], xh[2 * s], xh[2 * s + 1]);
         }
     }
 }
