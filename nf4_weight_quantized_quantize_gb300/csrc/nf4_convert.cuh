@@ -92,6 +92,26 @@ __device__ __forceinline__ bool report_converted(int st) {
 #endif
 }
 
+// Named barriers among the converter warps of a tcgen05 kernel (barrier 0 is __syncthreads).
+// and_all: every converter thread arrives, each with its predicate; returns
+// whether all of them were true.
+__device__ __forceinline__ bool converters_and_all(bool pred, int threads) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void converters_sync(int threads) {
+    asm volatile("bar.sync 2, %0;" ::"r"(threads) : "memory");
+}
+
 // Wait (bounded) for the copies a producer issued into the last `slots`
 // stages of its ring to land, so no TMA or cp.async write targets shared
 // memory after exit.

@@ -110,26 +110,6 @@ __device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint3
     mbar_wait(bar.drain(issuer), 0, err, &dummy, kErrTimeoutDrain);
 }
 
-// Named barriers among the converter warps (barrier 0 is __syncthreads).
-// and_all: every converter thread arrives, each with its predicate; returns
-// whether all of them were true.
-__device__ __forceinline__ bool converters_and_all(bool pred, int threads) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ void converters_sync(int threads) {
-    asm volatile("bar.sync 2, %0;" ::"r"(threads) : "memory");
-}
-
 // ============================================================ the kernel
 
 // Compile-time layout of one kernel instance: NX activation rows per tile
@@ -861,6 +841,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t
 
 cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
                               const uint8_t* packed, const float* absmax, int64_t F, void* y, cudaStream_t s) {
+    if (wide_applies(dtype, M, 2 * F)) return launch_gemm_wide(dev, dtype, x, M, K, packed, absmax, 2 * F, y, s, true);
     // ceil(2F / 128) tiles of 128 weight rows = ceil(F / 64) tiles of 64 gate/up row pairs
     const Plan p = make_plan(M, 2 * F, K);
     if (p.split) return cudaErrorInvalidValue;

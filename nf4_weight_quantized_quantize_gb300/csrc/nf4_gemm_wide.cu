@@ -21,6 +21,8 @@
 //     CTA this wide cannot hide the activation tiles' load latency within its
 //     shared memory: its MMA issuer waited on them about a quarter of the time).
 // The pair's tile is 256 weight rows x 2 NX activation rows over the whole K.
+// A gate/up pair (GEGLU) takes 64 gate rows and the 64 up rows of the same
+// outputs per CTA and writes gelu_tanh(gate) * up.
 //
 // Rings (per CTA): activations, SX slots of one K-slice (NX rows x 128 bytes:
 // the CTA's halves of both accumulators, TMA with the 128-byte swizzle);
@@ -81,6 +83,9 @@ struct WdCfg {
     static_assert(XS % 1024 == 0, "slot alignment");
     static_assert(SX >= 3, "activation ring depth");
     static_assert(SMEM <= kWdSmemLimit, "shared memory budget");
+    // a gate/up pair's epilogue parks half of each CTA's accumulator columns,
+    // [2 NX columns][64 pair rows] fp32, in the activation ring
+    static_assert(SX * XS >= 2 * NX * (BW / 2) * 4, "gate/up exchange buffer");
     // packed tile: rows of 64 bytes loaded with the 64-byte swizzle (16-byte
     // chunk c of row r at c ^ ((r / 2) % 4)), so a warp's reads of one chunk
     // from 32 rows spread over all banks
@@ -91,9 +96,9 @@ struct WdCfg {
 };
 
 struct WdArgs {
-    const float* absmax;   // [N, K / 64]
-    void* y;               // [M, N]
-    int M, N, K;
+    const float* absmax;   // [N, K / 64] ([2F, K / 64] for a gate/up pair)
+    void* y;               // [M, N] ([M, F] for a gate/up pair)
+    int M, N, K;           // N: output columns (F for a gate/up pair)
     int m_tiles;
     uint32_t* err;
 };
@@ -213,7 +218,10 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
-template <int NX, int DT>
+// GEGLU: the weight is a gate/up pair [2F, K] (gate rows first) and each
+// CTA's 128 weight rows are 64 gate rows and the 64 up rows of the same
+// outputs; the epilogue writes gelu_tanh(gate) * up, [M, F].
+template <int NX, int DT, bool GEGLU>
 __global__ void __launch_bounds__(kWdThreads, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const WdArgs args) {
     using C = WdCfg<NX>;
@@ -241,7 +249,10 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int pair = static_cast<int>(blockIdx.x >> 1);
     // pairs run m-fastest: pairs resident together share each weight tile through L2
     const int m0 = (pair % args.m_tiles) * (2 * NX);
-    const int n0 = (pair / args.m_tiles) * (2 * C::BW) + static_cast<int>(rank) * C::BW;   // this CTA's weight rows
+    // this CTA's first weight row (first gate row of a pair: the pair covers
+    // 128 outputs, 64 per CTA)
+    constexpr int kRowsOut = GEGLU ? C::BW / 2 : C::BW;
+    const int n0 = (pair / args.m_tiles) * (2 * kRowsOut) + static_cast<int>(rank) * kRowsOut;
     const int nk = args.K / kBK;
     const int nst = (nk + kWdKs - 1) / kWdKs;
 
@@ -324,9 +335,9 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             if (!__all_sync(0xffffffffu, ok && !*abort_flag)) break;
             const int kb = st * kWdKs;
             uint8_t* ptile = smem + C::OFF_P + p * C::P_SLOT;
-            produce_weights<C::BW, kWdKs, false>(pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(ptile),
-                                                 kb * kPackedRow, n0, 0, args.N, smem_u32(ptile + C::P_BYTES),
-                                                 args.absmax, nk, kb);
+            produce_weights<C::BW, kWdKs, GEGLU>(pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(ptile),
+                                                 kb * kPackedRow, n0, args.N + n0, args.N,
+                                                 smem_u32(ptile + C::P_BYTES), args.absmax, nk, kb);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(pfull(0), SP, issued, args.err);
@@ -450,25 +461,72 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
         // tcgen05.ld is warp-collective: decide for the whole warp
         ok = __all_sync(0xffffffffu, ok) && mbar_wait_cluster(accum, 0, args.err, abort_flag, kErrTimeoutAccum);
-        if (__all_sync(0xffffffffu, ok)) {
+        // accumulator acc: TMEM lane = weight row, column c = activation row
+        // m0 + acc NX + c (both CTAs' halves); chunk ci = 16 columns of
+        // accumulator ci / CHUNKS, chunks round-robin over the 4 units
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        constexpr int CHUNKS = NX / 16;
+        auto load_chunk = [&](int ci, uint32_t (&v)[16]) {
+            tmem_ld16(lane_addr + (ci / CHUNKS) * kWdAccStride + 16 * (ci % CHUNKS), v);
+            tmem_ld_wait();
+        };
+        auto col_row = [&](int ci, int i) { return m0 + (ci / CHUNKS) * NX + 16 * (ci % CHUNKS) + i; };
+        if constexpr (GEGLU) {
+            // Lanes 0-63 hold the gate rows n0 + r, lanes 64-127 the up rows of
+            // the same outputs.  Of a unit's chunks u, u + 4, u + 8, ... the gate
+            // warps (lane quarters 0-1) write u, u + 8, ... and the up warps
+            // u + 4, u + 12, ...: first each side parks its raw values of the
+            // chunks the other side writes in the activation ring (every TMA
+            // load into it was read by an MMA that has completed, the peer's
+            // included), then each side finishes its own chunks.  Every
+            // converter thread reaches both named barriers on every path.
+            constexpr int kConvThreads = 32 * kWdConvWarps;
+            const bool all_ok = converters_and_all(__all_sync(0xffffffffu, ok), kConvThreads);
+            float* xbuf = reinterpret_cast<float*>(smem);   // column c, pair row rr at c * 64 + rr
+            const bool gate = q < 2;
+            const int rr = gate ? r : r - C::BW / 2;
+            if (all_ok) {
+                tc_fence_after();
+                fence_proxy_async_smem();   // the ring was last written by TMA
+#pragma unroll 1
+                for (int ci = u + (gate ? 4 : 0); ci < 2 * CHUNKS; ci += 8) {
+                    uint32_t v[16];
+                    load_chunk(ci, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) xbuf[(16 * ci + i) * (C::BW / 2) + rr] = __uint_as_float(v[i]);
+                }
+            }
+            converters_sync(kConvThreads);
+            if (all_ok) {
+                const int n = n0 + rr;
+#pragma unroll 1
+                for (int ci = u + (gate ? 0 : 4); ci < 2 * CHUNKS; ci += 8) {
+                    uint32_t v[16];
+                    load_chunk(ci, v);
+                    if (n < args.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = col_row(ci, i);
+                            const float mine = __uint_as_float(v[i]);
+                            const float other = xbuf[(16 * ci + i) * (C::BW / 2) + rr];
+                            const float g = gate ? mine : other;
+                            const float up = gate ? other : mine;
+                            if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, gelu_tanh(g) * up);
+                        }
+                    }
+                }
+            }
+        } else if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
-            // accumulator acc: TMEM lane = weight row n0 + r, column c = activation
-            // row m0 + acc NX + c (both CTAs' halves); 16-column chunks round-robin
-            // over the 4 units
             const int n = n0 + r;
-            const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            constexpr int CHUNKS = NX / 16;
 #pragma unroll 1
             for (int ci = u; ci < 2 * CHUNKS; ci += 4) {
-                const int acc = ci / CHUNKS;
-                const int c0 = 16 * (ci % CHUNKS);
                 uint32_t v[16];
-                tmem_ld16(lane_addr + acc * kWdAccStride + c0, v);
-                tmem_ld_wait();
+                load_chunk(ci, v);
                 if (n < args.N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + acc * NX + c0 + i;
+                        const int m = col_row(ci, i);
                         if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, __uint_as_float(v[i]));
                     }
                 }
@@ -502,25 +560,28 @@ WdPlan make_wd_plan(int64_t M, int64_t N) {
     return p;
 }
 
-template <int NX, int DT>
+// N: rows of the weight (2F for a gate/up pair, whose output has F columns).
+template <int NX, int DT, bool GEGLU>
 cudaError_t launch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int64_t M, int64_t K,
                       const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
     using C = WdCfg<NX>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
-    auto kernel = wide_kernel<NX, DT>;
+    auto kernel = wide_kernel<NX, DT, GEGLU>;
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     CUtensorMap tm_x, tm_w;
     const CUtensorMapDataType xdt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     // activations: boxes of one K-slice (64 values, 128 bytes: the swizzle
     // span) x NX / 2 rows; packed weights: boxes of two K-slices x 128 rows
+    // (x 64 rows for a gate/up pair, one box of gate rows and one of up rows)
     if (!make_map(&tm_x, x, xdt, 2, M, K, NX / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, C::BW, kPackedRow * kWdKs,
-                  CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, GEGLU ? C::BW / 2 : C::BW,
+                  kPackedRow * kWdKs, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     const int64_t ctas = 2 * static_cast<int64_t>(p.m_tiles) * p.n_pairs;
     if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    WdArgs a{absmax, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.m_tiles, dev.err_word};
+    const int64_t n_out = GEGLU ? N / 2 : N;
+    WdArgs a{absmax, y, static_cast<int>(M), static_cast<int>(n_out), static_cast<int>(K), p.m_tiles, dev.err_word};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(kWdThreads);
@@ -540,14 +601,14 @@ cudaError_t launch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int
     return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, bool GEGLU>
 cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
     switch (p.nx) {
-        case 160: return launch_wd<160, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 192: return launch_wd<192, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 224: return launch_wd<224, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case 256: return launch_wd<256, DT>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case 160: return launch_wd<160, DT, GEGLU>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case 192: return launch_wd<192, DT, GEGLU>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case 224: return launch_wd<224, DT, GEGLU>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case 256: return launch_wd<256, DT, GEGLU>(dev, p, x, M, K, packed, absmax, N, y, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -573,11 +634,17 @@ bool wide_applies(int dtype, int64_t M, int64_t N) {
 }
 
 cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
-                             const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s) {
-    const WdPlan p = make_wd_plan(M, N);
+                             const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s,
+                             bool geglu) {
+    if (geglu && N % 2 != 0) return cudaErrorInvalidValue;
+    const WdPlan p = make_wd_plan(M, N);   // a pair of 256 weight rows = 128 gate/up row pairs
     switch (dtype) {
-        case kBF16: return dispatch_wd<kBF16>(dev, p, x, M, K, packed, absmax, N, y, s);
-        case kF16: return dispatch_wd<kF16>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case kBF16:
+            return geglu ? dispatch_wd<kBF16, true>(dev, p, x, M, K, packed, absmax, N, y, s)
+                         : dispatch_wd<kBF16, false>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case kF16:
+            return geglu ? dispatch_wd<kF16, true>(dev, p, x, M, K, packed, absmax, N, y, s)
+                         : dispatch_wd<kF16, false>(dev, p, x, M, K, packed, absmax, N, y, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -71,13 +71,16 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t
                         const uint8_t* packed, const float* absmax, int64_t N, void* y,
                         cudaStream_t s);
 
-// The wide NF4 GEMM (nf4_gemm_wide.cu): expanded weights in shared memory,
-// two TMEM accumulators, tiles of 128 weight rows x up to 512 activation
-// rows (bf16 / fp16, M > 256).  wide_applies: whether it beats the tile
-// kernel on this shape (a shape-only estimate); launch_gemm uses it then.
+// The CTA-pair NF4 GEMM (nf4_gemm_wide.cu): expanded weights in shared
+// memory, two TMEM accumulators, pair tiles of 256 weight rows x up to 512
+// activation rows (bf16 / fp16, M > 256).  wide_applies: whether it beats
+// the tile kernel on this shape (a shape-only estimate; N = rows of the
+// weight); launch_gemm and launch_gemm_geglu use it then.  N: rows of the
+// weight; geglu: the weight is a gate/up pair (N = 2F) and Y is [M, F].
 bool wide_applies(int dtype, int64_t M, int64_t N);
 cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
-                             const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s);
+                             const uint8_t* packed, const float* absmax, int64_t N, void* y, cudaStream_t s,
+                             bool geglu = false);
 
 // Workspace bytes the skinny (M < 128) path needs for this shape.
 size_t skinny_workspace_bytes(const DeviceInfo* dev, int64_t M, int64_t N, int64_t K);

@@ -153,13 +153,14 @@ def test_linear_f16(M, N, K):
     assert not (np.abs(ys - yref) > bound).any()
 
 
-@pytest.mark.parametrize("M", [300, 16])
-def test_linear_geglu_f16(M):
-    F, K = 640, 1024
+@pytest.mark.parametrize("M,F,K", [(300, 640, 1024), (16, 640, 1024), (2048, 2432, 256)],
+                         ids=["tile_tcgen05", "warp_mma", "cta_pair"])
+def test_linear_geglu_f16(M, F, K):
     w = rand_w(2 * F * K, 0.05, 90 + M, "f16").reshape(2 * F, K)
     x = rand_w(M * K, 1.0, 91 + M, "f16").reshape(M, K)
+    rows = None if M * F <= 1 << 20 else np.sort(np.random.default_rng(M).choice(M, 32, replace=False))
     f16_linear_check(x, w, lambda xd, pd, ad: nf4.linear_geglu(xd, pd, ad, F), F,
-                     lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f16"))
+                     lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f16"), rows)
 
 
 @pytest.mark.parametrize("M", [16, 64, 300], ids=["warp_mma", "split_tcgen05", "tile_tcgen05"])

@@ -100,6 +100,21 @@ def test_tile_path_ragged_shapes(M, F, K):
     check(rand_bits((M, K), 1.0, 3 * M + K), w)
 
 
+@pytest.mark.parametrize("M,F,K", [
+    (2048, 2432, 128),   # 19 pair tiles of 128 outputs x 4 tiles of 512 activation rows
+    (1500, 2400, 320),   # ragged M and F (the last CTA's outputs partly past F), 5 K-slices
+    (640, 4800, 192),    # 160 activation rows per accumulator, 3 K-slices
+])
+def test_pair_kernel_shapes(M, F, K):
+    """Shapes the CTA-pair kernel takes (64 gate and 64 up rows per CTA, the
+    epilogue exchanging halves through shared memory), on sampled rows."""
+    w = Pair(rand_bits((2 * F, K), 0.05, M + 7 * F))
+    rows = np.sort(np.random.default_rng(M + F).choice(M, 48, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    y = check(rand_bits((M, K), 1.0, 5 * M + K), w, rows=rows)
+    assert np.array_equal(y, run(rand_bits((M, K), 1.0, 5 * M + K), w))
+
+
 @pytest.mark.parametrize("M", [1, 7, 16, 17, 64, 100, 127])
 def test_skinny_path_widths(M):
     F, K = 320, 1536
