@@ -8,6 +8,7 @@
 
 #include <bit>
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -248,6 +249,36 @@ __device__ __forceinline__ void store_out(void* y, int64_t i, float v) {
         static_cast<float*>(y)[i] = v;
     else
         static_cast<uint16_t*>(y)[i] = round16<DT>(v);
+}
+
+// Store 16 values of output column n, rows m_first .. m_first + 15 of a
+// row-major output with `ld` columns, rounded to DT (fp32: as they are).
+// One pointer advanced by a row per value; the row bound is checked once
+// for the whole run unless it ends past M.  (Indexing every element from
+// (m, n) cost the GEMM epilogues about half their time.)
+template <int DT>
+__device__ __forceinline__ void store_col16(void* y, int64_t ld, int m_first, int M, int n, const float (&v)[16]) {
+    using E = typename std::conditional<DT == kF32, float, uint16_t>::type;
+    E* p = static_cast<E*>(y) + static_cast<int64_t>(m_first) * ld + n;
+    auto cvt = [](float x) -> E {
+        if constexpr (DT == kF32)
+            return x;
+        else
+            return round16<DT>(x);
+    };
+    if (m_first + 15 < M) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            *p = cvt(v[i]);
+            p += ld;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (m_first + i < M) *p = cvt(v[i]);
+            p += ld;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- dependent launch

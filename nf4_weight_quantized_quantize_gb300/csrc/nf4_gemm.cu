@@ -542,15 +542,14 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     uint32_t v[16];
                     load_acc(c0, v);
                     if (n < args.N) {
+                        float o[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const int m = m0 + c0 + i;
                             const float mine = __uint_as_float(v[i]);
                             const float other = xbuf[(c0 + i) * HW + rr];
-                            const float g = gate ? mine : other;
-                            const float up = gate ? other : mine;
-                            if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, gelu_tanh(g) * up);
+                            o[i] = gate ? gelu_tanh(mine) * other : gelu_tanh(other) * mine;
                         }
+                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o);
                     }
                 }
             }
@@ -564,17 +563,14 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 uint32_t v[16];
                 load_acc(c0, v);
                 if (n < args.N) {
+                    float o[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + c0 + i;
-                        if (m < args.M) {
-                            if constexpr (SPLIT) {
-                                args.ws[(static_cast<int64_t>(split) * args.M + m) * args.N + n] = __uint_as_float(v[i]);
-                            } else {
-                                store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, __uint_as_float(v[i]));
-                            }
-                        }
-                    }
+                    for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[i]);
+                    if constexpr (SPLIT)   // this split's fp32 partial, [splits][M][N]
+                        store_col16<kF32>(args.ws + static_cast<int64_t>(split) * args.M * args.N, args.N, m0 + c0,
+                                          args.M, n, o);
+                    else
+                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o);
                 }
             }
         }

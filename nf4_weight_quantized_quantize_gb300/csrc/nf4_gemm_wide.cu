@@ -470,7 +470,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             tmem_ld16(lane_addr + (ci / CHUNKS) * kWdAccStride + 16 * (ci % CHUNKS), v);
             tmem_ld_wait();
         };
-        auto col_row = [&](int ci, int i) { return m0 + (ci / CHUNKS) * NX + 16 * (ci % CHUNKS) + i; };
+        auto col_row = [&](int ci, int i) { return m0 + (ci / CHUNKS) * NX + 16 * (ci % CHUNKS) + i; };   // activation row
         if constexpr (GEGLU) {
             // Lanes 0-63 hold the gate rows n0 + r, lanes 64-127 the up rows of
             // the same outputs.  Of a unit's chunks u, u + 4, u + 8, ... the gate
@@ -504,15 +504,14 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     uint32_t v[16];
                     load_chunk(ci, v);
                     if (n < args.N) {
+                        float o[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const int m = col_row(ci, i);
                             const float mine = __uint_as_float(v[i]);
                             const float other = xbuf[(16 * ci + i) * (C::BW / 2) + rr];
-                            const float g = gate ? mine : other;
-                            const float up = gate ? other : mine;
-                            if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, gelu_tanh(g) * up);
+                            o[i] = gate ? gelu_tanh(mine) * other : gelu_tanh(other) * mine;
                         }
+                        store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o);
                     }
                 }
             }
@@ -524,11 +523,10 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 uint32_t v[16];
                 load_chunk(ci, v);
                 if (n < args.N) {
+                    float o[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = col_row(ci, i);
-                        if (m < args.M) store_out<DT>(args.y, static_cast<int64_t>(m) * args.N + n, __uint_as_float(v[i]));
-                    }
+                    for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[i]);
+                    store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o);
                 }
             }
         }
