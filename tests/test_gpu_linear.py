@@ -156,10 +156,11 @@ def test_tile_path_larger_shapes(M, N, K):
     (1500, 10000, 192),    # ragged M (the last tile's second accumulator half partly past M) and N, odd block count
     (2047, 4100, 320),     # 4 tiles of 512 rows, the last one ragged; a partial weight tile
     (4096, 2048, 128),     # 8 tiles of 512 rows, one stage
+    (2000, 20000, 256),    # 316 pair tiles (632 CTAs, several waves), ragged M and N
 ])
 def test_wide_path_shapes(M, N, K):
-    """Shapes the two-accumulator kernel takes (expanded weights in shared
-    memory, tiles of 128 x 512): against the oracle on sampled rows, plus
+    """Shapes the CTA-pair kernel takes (expanded weights in shared memory,
+    pair tiles of 256 x 512): against the oracle on sampled rows, plus
     determinism."""
     q = Quantized(rand_bits((N, K), 0.02, M + 5 * N))
     x_bits = rand_bits((M, K), 1.0, K + 2 * M)
