@@ -138,7 +138,7 @@ def f16_linear_check(x_cpu, w_cpu, fn, n_cols, oracle_fn, rows=None):
 
 
 @pytest.mark.parametrize("M,N,K", [(2048, 4096, 3840), (16, 3840, 15360), (257, 300, 128), (130, 640, 1536),
-                                   (33, 1000, 64 * 50)])
+                                   (33, 1000, 64 * 50), (700, 30720, 128)])
 def test_linear_f16(M, N, K):
     rs_seed = M + N + K
     w = rand_w(N * K, 0.02, rs_seed, "f16").reshape(N, K)

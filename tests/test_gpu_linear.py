@@ -157,6 +157,9 @@ def test_tile_path_larger_shapes(M, N, K):
     (2047, 4100, 320),     # 4 tiles of 512 rows, the last one ragged; a partial weight tile
     (4096, 2048, 128),     # 8 tiles of 512 rows, one stage
     (2000, 20000, 256),    # 316 pair tiles (632 CTAs, several waves), ragged M and N
+    (300, 10000, 128),     # 160 activation rows per accumulator, the second one partly past M
+    (700, 30720, 192),     # 192 rows per accumulator, 2 tiles of 350 rows
+    (850, 30720, 128),     # 224 rows per accumulator, 2 tiles of 425 rows
 ])
 def test_wide_path_shapes(M, N, K):
     """Shapes the CTA-pair kernel takes (expanded weights in shared memory,
