@@ -102,13 +102,11 @@ __device__ __forceinline__ void init_barriers(const Barriers& bar, int conv_arri
     mbar_init(bar.drain(1), 1);
 }
 
-// Error-path exit of an MMA issuer: wait (bounded) until every MMA it issued
-// has completed, so TMEM can be released.
-__device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer, uint32_t* err) {
-    int dummy = 0;
-    mma_commit(bar.drain(issuer));
-    mbar_wait(bar.drain(issuer), 0, err, &dummy, kErrTimeoutDrain);
-}
+// Exit of an MMA issuer: commit every MMA it issued to its drain barrier.
+// The TMEM owner waits on it (bounded, whatever the CTA's abort flag says)
+// before releasing TMEM, so TMEM is never freed under a running MMA, on any
+// path (converters that gave up skip their wait on the accumulators).
+__device__ __forceinline__ void drain_mma(const Barriers& bar, int issuer) { mma_commit(bar.drain(issuer)); }
 
 // ============================================================ the kernel
 
@@ -383,10 +381,8 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 }
                 mma_commit(bar.done(t));
             }
-            if (ok)
-                mma_commit(bar.accum());
-            else
-                drain_mma(bar, issuer, args.err);
+            if (ok) mma_commit(bar.accum());
+            drain_mma(bar, issuer);   // on every path (see drain_mma)
         }
     } else {
         // ---------------- converters: unit u = (warp - 2) / 4 converts part
@@ -579,6 +575,9 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        // every MMA of the CTA has completed (each issuer committed to its drain)
+        int dummy = 0;
+        for (int i = 0; i < C::MI; ++i) mbar_wait(bar.drain(i), 0, args.err, &dummy, kErrTimeoutDrain);
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }

@@ -372,13 +372,12 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 mma_commit_pair(xempty(x));
                 mma_commit_pair(aempty(a));
             }
-            if (ok) {
-                mma_commit_pair(accum);
-            } else {
-                int dummy = 0;
-                mma_commit_pair(drain);
-                mbar_wait(drain, 0, args.err, &dummy, kErrTimeoutDrain);
-            }
+            if (ok) mma_commit_pair(accum);
+            // On every path, the pair's MMAs committed to both CTAs' drain
+            // barriers: warp 1 of each CTA waits on it before releasing TMEM,
+            // so TMEM is never freed under a running MMA (converters that gave
+            // up skip their wait on accum).
+            mma_commit_pair(drain);
         }
     } else {
         // ---------------- converters: unit u = (warp - 2) / 4 expands half
@@ -536,6 +535,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     __syncthreads();
     cluster_sync_all();   // the pair is done with both TMEMs before either frees them
     if (warp == 1) {
+        int dummy = 0;   // bounded, whatever the abort flag says: the pair's MMAs have completed
+        mbar_wait(drain, 0, args.err, &dummy, kErrTimeoutDrain);
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);
     }
