@@ -275,18 +275,21 @@ def test_small_batch_kernel_shapes(M, N, K):
     assert np.array_equal(y1, run_linear(x_bits, q))     # deterministic: fixed split order
 
 
-@pytest.mark.parametrize("M", [16, 64, 256], ids=["warp_mma", "split_tcgen05", "tile_tcgen05"])
-def test_absmax_not_a_bf16_value(M):
+@pytest.mark.parametrize("M,N", [(16, 384), (64, 384), (256, 384), (2048, 4864)],
+                         ids=["warp_mma", "split_tcgen05", "tile_tcgen05", "cta_pair"])
+def test_absmax_not_a_bf16_value(M, N):
     """Scales that are not bf16 values (a weight quantized at fp32, then used
     at bf16): every kernel path must still multiply by the exact fp32 absmax
-    and round once, which is what nf4_dequantize (and the oracle) compute."""
-    N, K = 384, 1024
+    and round once, which is what nf4_dequantize (and the oracle) compute
+    (sampled rows for the large batch)."""
+    K = 1024
     q = Quantized(rand_bits((N, K), 0.02, 21))
     bumped = (q.a.view(np.uint32) | np.uint32(0x5a5)).view(np.float32)   # low fraction bits set
     q.a = bumped.copy()
     q.ad = torch.from_numpy(q.a).to(DEV)
     q._wdeq = None
-    check(rand_bits((M, K), 1.0, 22), q)
+    rows = None if M <= 256 else np.sort(np.random.default_rng(M).choice(M, 32, replace=False))
+    check(rand_bits((M, K), 1.0, 22), q, rows=rows)
 
 
 def test_no_error_recorded():
