@@ -153,8 +153,11 @@ NF4_API nf4_status nf4_dequantize(const uint8_t* packed, const float* absmax, in
  * quantized at fp32).  Not bit-exact: the fp32 accumulation order is the
  * kernel's, but repeated calls on the same inputs give the same bits; the
  * result matches an fp64 matmul of the dequantized weights to within bf16
- * output rounding plus fp32 summation error.  Rows of Y are independent of
- * each other.  After NF4_ERR_TIMEOUT (see nf4_last_error) y is undefined.
+ * output rounding plus fp32 summation error.  Row m of Y depends only on row
+ * m of X and on the weight, but the kernel -- and with it the fp32 summation
+ * order -- is chosen by the shape, so the same row computed in a call with
+ * another M may differ in its last bits.  After NF4_ERR_TIMEOUT (see
+ * nf4_last_error) y is undefined.
  */
 NF4_API nf4_status nf4_linear(const uint16_t* x, int64_t M, int64_t K, const uint8_t* packed,
                       const float* absmax, int64_t N, int32_t block, uint16_t* y,

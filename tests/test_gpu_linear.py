@@ -111,8 +111,9 @@ def test_down_proj_skinny_full():
 
 
 def test_skinny_rows_equal_rows_of_full_batch():
-    """Batched-vs-solo: the 16-row call (skinny kernel) matches the same 16 rows
-    of the 2048-row call (tile kernel) to within fp32 reordering + bf16 rounding."""
+    """Batched-vs-solo: the 16-row call (warp-MMA kernel) matches the same 16
+    rows of the 2048-row call (CTA-pair kernel) to within fp32 reordering +
+    bf16 rounding."""
     q = Quantized(workloads.bits(workloads.make_weight(workloads.DOWN)))
     xf = workloads.bits(workloads.make_activation(workloads.DOWN))
     xs = workloads.bits(workloads.make_activation(workloads.DOWN_SKINNY))
