@@ -29,9 +29,10 @@
 // expanded weights, SA slots of one K-slice written by the converters;
 // packed weights, SP slots of two K-slices of packed bytes and fp32 scales.
 // Warps: 0 loads activations (both CTAs' copies complete on the even CTA's
-// barrier); 1 allocates TMEM (both CTAs) and in the even CTA issues the
-// MMAs; 2-17 are converters (both CTAs' arrive on the even CTA's barrier),
-// then the epilogue; 18 loads packed weights.  MMA completion is
+// barrier); 1 allocates TMEM (both CTAs) and in the even CTA issues the first
+// accumulator's MMAs; 2-17 are converters (both CTAs' arrive on the even
+// CTA's barrier), then the epilogue; 18 loads packed weights; 19 (even CTA)
+// issues the second accumulator's MMAs.  MMA completion is
 // committed to the barriers of both CTAs.  Every wait is bounded
 // (NF4_WAIT_LIMIT_NS); on expiry the CTA records an error code, drains what it
 // has in flight and frees TMEM, and the peer's waits on it expire in turn.
@@ -54,7 +55,9 @@ namespace {
 constexpr int kWdKs = 2;                               // K-slices per stage
 constexpr int kWdConvWarps = 16;                       // 4 lane quarters x 2 K-slices x 2 halves
 constexpr int kWdWprodWarp = 2 + kWdConvWarps;         // 18
-constexpr int kWdThreads = 32 * (kWdWprodWarp + 1);    // 608
+constexpr int kWdIssuer1Warp = kWdWprodWarp + 1;       // 19: the second accumulator's MMA issuer
+constexpr int kWdThreads = 32 * (kWdIssuer1Warp + 1);  // 640
+constexpr int kWdIssuers = 2;                          // one MMA issuer thread per accumulator
 constexpr uint64_t kWdSettleNs = 1000000;              // error path: time for copies in flight to land
 constexpr int kWdSmemLimit = 232448;
 constexpr int kWdAccStride = 256;                      // TMEM columns between the two accumulators
@@ -257,20 +260,22 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int nst = (nk + kWdKs - 1) / kWdKs;
 
     if (threadIdx.x == 0) {
+        // the MMA commits of both issuers release a slot, complete the
+        // accumulators, drain
         for (int i = 0; i < SX; ++i) {
             mbar_init(xfull(i), 1);
-            mbar_init(xempty(i), 1);
+            mbar_init(xempty(i), kWdIssuers);
         }
         for (int i = 0; i < SA; ++i) {
             mbar_init(afull(i), kWdConvWarps);   // (even CTA) the 8 warps per CTA that expand a K-slice
-            mbar_init(aempty(i), 1);
+            mbar_init(aempty(i), kWdIssuers);
         }
         for (int i = 0; i < SP; ++i) {
             mbar_init(pfull(i), kPfullArrivals);
             mbar_init(pempty(i), kWdConvWarps);
         }
-        mbar_init(accum, 1);
-        mbar_init(drain, 1);
+        mbar_init(accum, kWdIssuers);
+        mbar_init(drain, kWdIssuers);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -341,15 +346,25 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(pfull(0), SP, issued, args.err);
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kWdIssuer1Warp) {
         if (lane == 0 && rank == 0) {
-            // ---------------- MMA issuer of the pair: per K-slice, wait until
-            // both CTAs expanded its weights and both CTAs' activation halves
-            // landed; 4 k-steps x 2 accumulators; commits to both CTAs that
-            // release the K-slice's activation and expanded-weight slots
+            // ---------------- MMA issuers of the pair, one thread per
+            // accumulator (warp 1: activation rows m0 .. m0 + NX - 1, warp 19:
+            // the next NX), each in a warp of its own: a single thread issuing
+            // both accumulators' MMAs, with its two barrier checks per K-slice,
+            // took about 0.7 us per K-slice against 0.5 us of tensor work.  Per
+            // K-slice each waits until both CTAs expanded its weights and both
+            // CTAs' activation halves landed, issues its 4 k-steps and commits
+            // to both CTAs' barriers that release the K-slice's activation and
+            // expanded-weight slots (each counts both issuers' commits).
+            const int acc = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16kind_f32<DT>(256, NX);
-            const uint32_t a_base = smem_u32(smem + C::OFF_A);
-            const uint32_t x_base = smem_u32(smem);
+            // descriptors of slot 0, k-step 0; a slot or a k-step adds to the
+            // 14-bit start-address field (address / 16), which never carries:
+            // shared-memory addresses stay below 2^18
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + C::OFF_A));
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem) + acc * HX * 128);
+            const uint32_t d_tmem = tmem + acc * kWdAccStride;
             bool ok = true;
             for (int k = 0; k < nk; ++k) {
                 const int a = k % SA;
@@ -358,25 +373,19 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                      mbar_wait_cluster(xfull(x), (k / SX) & 1, args.err, abort_flag, kErrTimeoutFull);
                 if (!ok) break;
                 tc_fence_after();
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((a * C::A_KS) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((x * C::XS) >> 4);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // k-step j of the K-slice: 32 bytes of each row
-                    const uint64_t adesc = smem_desc_sw128(a_base + a * C::A_KS + 32 * j);
-#pragma unroll
-                    for (int acc = 0; acc < 2; ++acc) {
-                        const uint64_t bdesc = smem_desc_sw128(x_base + x * C::XS + acc * HX * 128 + 32 * j);
-                        const uint32_t first = (k == 0 && j == 0) ? 0u : 1u;
-                        mma_pair(tmem + acc * kWdAccStride, adesc, bdesc, idesc, first);
-                    }
-                }
+                for (int j = 0; j < 4; ++j)   // k-step j of the K-slice: 32 bytes of each row
+                    mma_pair(d_tmem, ad + 2 * j, bd + 2 * j, idesc, (k == 0 && j == 0) ? 0u : 1u);
                 mma_commit_pair(xempty(x));
                 mma_commit_pair(aempty(a));
             }
             if (ok) mma_commit_pair(accum);
-            // On every path, the pair's MMAs committed to both CTAs' drain
-            // barriers: warp 1 of each CTA waits on it before releasing TMEM,
-            // so TMEM is never freed under a running MMA (converters that gave
-            // up skip their wait on accum).
+            // On every path, the MMAs committed to both CTAs' drain barriers:
+            // warp 1 of each CTA waits on it before releasing TMEM, so TMEM is
+            // never freed under a running MMA (converters that gave up skip
+            // their wait on accum).
             mma_commit_pair(drain);
         }
     } else {
