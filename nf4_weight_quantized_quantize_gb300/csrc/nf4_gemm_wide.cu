@@ -626,9 +626,10 @@ cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, i
 // Whether the pair kernel takes this call, by a shape-only estimate of both
 // kernels' time: waves of one CTA per SM times the time of a K-slice.  Measured
 // on GB300 at M = 2048 (bf16, L2 flushed): about 0.52 us (1000 clocks) per
-// K-slice for the tile kernel's 128 x 256 tile and 0.81 us (1560 clocks) for a
-// pair's 256 x 512 tile at nx = 256 -- its MMAs scale with nx, its converters
-// and signalling do not, so smaller nx is not taken below the tile kernel's.
+// K-slice for the tile kernel's 128 x 256 tile, and 0.53 us (1060 clocks, the
+// slope of time over K) for a pair's 256 x 512 tile at nx = 256, the tensor
+// rate -- its MMAs scale with nx, its converters and signalling do not, so
+// smaller nx is not taken below the tile kernel's.
 bool wide_applies(int dtype, int64_t M, int64_t N) {
     if ((dtype != kBF16 && dtype != kF16) || M <= 256) return false;
     const WdPlan p = make_wd_plan(M, N);
@@ -637,7 +638,7 @@ bool wide_applies(int dtype, int64_t M, int64_t N) {
     const double n_tiles = std::ceil(N / 128.0);
     const double ts_waves = std::ceil(n_tiles * std::ceil(M / 256.0) / kSms);
     const double wd_waves = std::ceil(2.0 * p.n_pairs * p.m_tiles / kSms);
-    const double wd_slice = std::max(1000.0, 1560.0 * p.nx / 256.0);
+    const double wd_slice = std::max(1000.0, 1060.0 * p.nx / 256.0);
     return wd_waves * wd_slice < ts_waves * 1000.0;
 }
 
