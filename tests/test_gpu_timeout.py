@@ -37,6 +37,8 @@ def faulty_lib():
     P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
     lib.nf4_linear.argtypes = [P, I64, I64, P, P, I64, I32, P, P, SZ, P]
     lib.nf4_linear.restype = ctypes.c_int
+    lib.nf4_linear_geglu.argtypes = [P, I64, I64, P, P, I64, I32, P, P, SZ, P]
+    lib.nf4_linear_geglu.restype = ctypes.c_int
     lib.nf4_last_error.argtypes = [P]
     lib.nf4_last_error.restype = ctypes.c_int
     return lib
@@ -71,6 +73,20 @@ def test_bounded_wait_expires_and_reports(faulty_lib, m, n, k):
     assert st == nf4.NF4_OK                                  # the launch itself is fine
     assert faulty_lib.nf4_last_error(stream) == nf4.NF4_ERR_TIMEOUT
     assert faulty_lib.nf4_last_error(stream) == nf4.NF4_OK  # read-and-clear
+
+
+@pytest.mark.parametrize("m,f,k", [(256, 256, 512), (1500, 5000, 192)], ids=["tile_kernel", "pair_kernel"])
+def test_gate_up_pair_bounded_wait_expires(faulty_lib, m, f, k):
+    """The fused gate/up forms: their epilogues meet at named barriers, which
+    every converter thread must reach even when a wait ran out."""
+    x, pd, ad, _, _, _ = _inputs(m, 2 * f, k, m + f)
+    y = torch.empty(m, f, dtype=torch.bfloat16, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = faulty_lib.nf4_linear_geglu(x.data_ptr(), m, k, pd.data_ptr(), ad.data_ptr(), f, 64, y.data_ptr(),
+                                     None, 0, stream)
+    assert st == nf4.NF4_OK
+    assert faulty_lib.nf4_last_error(stream) == nf4.NF4_ERR_TIMEOUT
+    assert faulty_lib.nf4_last_error(stream) == nf4.NF4_OK
 
 
 def test_context_usable_after_timeouts(faulty_lib):
