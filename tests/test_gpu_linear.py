@@ -161,6 +161,7 @@ def test_tile_path_larger_shapes(M, N, K):
     (300, 10000, 128),     # 160 activation rows per accumulator, the second one partly past M
     (700, 30720, 192),     # 192 rows per accumulator, 2 tiles of 350 rows
     (850, 30720, 128),     # 224 rows per accumulator, 2 tiles of 425 rows
+    (2048, 4864, 64),      # one K-slice: one stage, its second half empty
 ])
 def test_wide_path_shapes(M, N, K):
     """Shapes the CTA-pair kernel takes (expanded weights in shared memory,
