@@ -294,6 +294,29 @@ def test_absmax_not_a_bf16_value(M, N):
     check(rand_bits((M, K), 1.0, 22), q, rows=rows)
 
 
+@pytest.mark.parametrize("cfg,reps", [(workloads.Q_PROJ, 100), (workloads.GATE_UP, 20)], ids=["q_proj", "gate_up"])
+def test_pair_kernel_repeatable_under_load(cfg, reps):
+    """Back-to-back calls of the CTA-pair kernel on the Gemma3 shapes at
+    M = 2048 (one wave, and several), each into its own output: every result
+    equals the first bit for bit.  The kernel is deterministic, so a read of
+    an expanded-weight or activation slot before its writes were visible --
+    the odd CTA signals the even one with a CTA-scope release -- would show
+    here as a rare difference."""
+    w = workloads.make_weight(cfg, device=DEV)
+    p, a = nf4.quantize(w)
+    del w
+    x = workloads.make_activation(cfg, device=DEV)
+    ref = nf4.linear(x, p, a, cfg.n)
+    outs = [torch.empty_like(ref) for _ in range(4)]
+    for i in range(reps):
+        nf4.linear(x, p, a, cfg.n, out=outs[i % 4])
+        if i % 4 == 3:
+            torch.cuda.synchronize()
+            for o in outs:
+                assert torch.equal(o, ref)
+    assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
+
+
 def test_no_error_recorded():
     assert nf4.nf4_last_error(torch.cuda.current_stream().cuda_stream) == nf4.NF4_OK
 
