@@ -46,6 +46,14 @@
  *     limit (about one second) records NF4_ERR_TIMEOUT in the device error word
  *     and exits early; nf4_last_error() reports it.  No call aborts the
  *     process or throws.
+ *   - Checked build (compiled with -DNF4_CHECKED; the library's build script
+ *     makes it on request, never as the default libnf4.so): every kernel
+ *     access to global memory that is not a TMA tensor copy first tests its
+ *     index against the extent of the buffer it addresses.  An index outside
+ *     skips the access and records NF4_ERR_BOUNDS, which nf4_last_error()
+ *     reports; the outputs are then undefined.  On valid arguments the
+ *     checked build computes the same bits as the normal one and reports
+ *     nothing.  The normal build contains no such test.
  *   - The current CUDA device must be an sm_103 GPU (else NF4_ERR_DEVICE).
  *   - Per device the library resolves, on its first call there, the device
  *     addresses of its own __device__ objects (the error word, and the scratch
@@ -79,7 +87,8 @@ typedef enum nf4_status {
     NF4_ERR_DEVICE = 6,     /* no current device, or it is not sm_103 */
     NF4_ERR_CUDA = 7,       /* a CUDA runtime call or launch failed */
     NF4_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by nf4_last_error) */
-    NF4_ERR_DTYPE = 9       /* an nf4_dtype this entry point does not take */
+    NF4_ERR_DTYPE = 9,      /* an nf4_dtype this entry point does not take */
+    NF4_ERR_BOUNDS = 10     /* checked build only: a kernel index fell outside its buffer (nf4_last_error) */
 } nf4_status;
 
 /* Compute dtypes of the _ex entry points. */
@@ -272,9 +281,11 @@ NF4_API nf4_status nf4_linear_noalloc(const uint16_t* x, int64_t M, int64_t K, c
                                       const float* absmax, int64_t N, int32_t block, uint16_t* y,
                                       void* stream);
 
-/* Synchronize `stream`, then read and clear this device's error word.
- * Returns NF4_OK, NF4_ERR_TIMEOUT (a kernel gave up on a wait), or
- * NF4_ERR_CUDA if the synchronization itself failed. */
+/* Synchronize `stream`, then read and clear this device's error word (the
+ * first error any kernel recorded since the last read).  Returns NF4_OK,
+ * NF4_ERR_TIMEOUT (a kernel gave up on a wait), NF4_ERR_BOUNDS (checked build:
+ * an index outside its buffer), or NF4_ERR_CUDA if the synchronization itself
+ * failed. */
 NF4_API nf4_status nf4_last_error(void* stream);
 
 /* Static, NUL-terminated name of a status code ("NF4_OK", ...). */

@@ -37,6 +37,7 @@ NF4_ERR_DEVICE = 6
 NF4_ERR_CUDA = 7
 NF4_ERR_TIMEOUT = 8
 NF4_ERR_DTYPE = 9
+NF4_ERR_BOUNDS = 10
 NF4_DTYPE_BF16 = 0
 NF4_DTYPE_F16 = 1
 NF4_DTYPE_F32 = 2
@@ -44,12 +45,10 @@ BLOCK = 64
 LIB_PATH = _build.LIB
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(
-            f"libnf4.so is not built ({LIB_PATH}); run "
-            "`python -m nf4_weight_quantized_quantize_gb300.build` first")
-    lib = ctypes.CDLL(LIB_PATH)
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of libnf4 at `path` with every entry point's signature set
+    (the bounds-checked build, for instance)."""
+    lib = ctypes.CDLL(path)
     P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
     sigs = {
         "nf4_quantize": [P, I64, I32, P, P, P],
@@ -74,6 +73,14 @@ def _load():
     lib.nf4_status_string.restype = ctypes.c_char_p
     lib.nf4_launch_count.restype = ctypes.c_uint64
     return lib
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libnf4.so is not built ({LIB_PATH}); run "
+            "`python -m nf4_weight_quantized_quantize_gb300.build` first")
+    return load_library(LIB_PATH)
 
 
 _lib = None

@@ -6,7 +6,12 @@ into ``libnf4.so`` beside this file.  No cmake, no setuptools; the CUDA driver A
 is reached through cudaGetDriverEntryPointByVersion, so the library has no
 link-time dependency on libcuda and loads on a machine without a GPU.
 
-    python -m nf4_weight_quantized_quantize_gb300.build [--force]
+``--checked`` builds ``_build/libnf4_checked.so`` instead (-DNF4_CHECKED):
+every kernel access that is not a TMA tensor copy tests its index against its
+buffer and reports NF4_ERR_BOUNDS through nf4_last_error() instead of
+touching memory outside it.  A debugging build, never the default library.
+
+    python -m nf4_weight_quantized_quantize_gb300.build [--force] [--checked]
 """
 from __future__ import annotations
 
@@ -23,6 +28,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnf4.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
+CHECKED_LIB = os.path.join(BUILD, "libnf4_checked.so")
+CHECKED_FLAGS = ["-DNF4_CHECKED"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -100,6 +107,10 @@ if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
+    ap.add_argument("--checked", action="store_true", help="build the bounds-checked library")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    if a.checked:
+        print(build(force=a.force, verbose=a.verbose, extra=CHECKED_FLAGS, out=CHECKED_LIB))
+    else:
+        print(build(force=a.force, verbose=a.verbose))
     sys.exit(0)

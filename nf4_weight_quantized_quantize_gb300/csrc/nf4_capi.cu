@@ -3,7 +3,7 @@
 // Validates arguments on the host, picks the kernel path and enqueues it on
 // the caller's stream.  Per device it keeps the device properties and the
 // address of a 4-byte error word that kernels set when a bounded wait gives
-// up.  Nothing here allocates device memory.
+// up (or, in the checked build, when an index falls outside its buffer).  Nothing here allocates device memory.
 #include <atomic>
 #include <mutex>
 
@@ -216,7 +216,8 @@ nf4_status nf4_last_error(void* stream) {
         cudaGetLastError();
         return NF4_ERR_CUDA;
     }
-    return word == 0 ? NF4_OK : NF4_ERR_TIMEOUT;
+    if (word == 0) return NF4_OK;
+    return (word >> 8) == (nf4::kErrBounds >> 8) ? NF4_ERR_BOUNDS : NF4_ERR_TIMEOUT;
 }
 
 const char* nf4_status_string(nf4_status status) {
@@ -231,6 +232,7 @@ const char* nf4_status_string(nf4_status status) {
         case NF4_ERR_CUDA: return "NF4_ERR_CUDA";
         case NF4_ERR_TIMEOUT: return "NF4_ERR_TIMEOUT";
         case NF4_ERR_DTYPE: return "NF4_ERR_DTYPE";
+        case NF4_ERR_BOUNDS: return "NF4_ERR_BOUNDS";
     }
     return "NF4_ERR_UNKNOWN";
 }

@@ -129,11 +129,12 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, int slots, int issued,
 // am_dst[h][row] -- and arrives on pfull[p] when its copies land.  Rows of a
 // box at or past n_lim (the rows of one half) and K-slices past the weight's
 // last block copy a harmless in-range scale (their products are never stored
-// or multiply zeros).
+// or multiply zeros).  absmax holds am_extent scales.
 template <int ROWS, int KS, bool PAIR>
 __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_t tx_bytes, const CUtensorMap* tm_w,
                                                 uint32_t p_dst, int p_col0, int n0, int n1, int n_lim,
-                                                uint32_t am_dst, const float* absmax, int am_pitch, int kb_abs0) {
+                                                uint32_t am_dst, const float* absmax, int am_pitch, int kb_abs0,
+                                                int64_t am_extent, uint32_t* err) {
     constexpr int H = PAIR ? ROWS / 2 : ROWS;   // rows per box
     if (lane == 0) {
         mbar_arrive_expect_tx(full, tx_bytes);
@@ -148,8 +149,8 @@ __device__ __forceinline__ void produce_weights(uint32_t full, int lane, uint32_
             const int il = i < H ? i : i - H;          // row within its box
             const int n = (i < H ? n0 : n1) + il;
             const bool ok = n0 + il < n_lim && kb_ok;
-            const float* src = absmax + (ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0);
-            cp_async_4(am_dst + 4u * (h * ROWS + i), src);
+            const int64_t src = ok ? static_cast<int64_t>(n) * am_pitch + kb_abs0 + h : 0;
+            if (in_bounds(err, src, am_extent)) cp_async_4(am_dst + 4u * (h * ROWS + i), absmax + src);
         }
     }
     cp_async_arrive_noinc(full);

@@ -15,6 +15,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "nf4_launch.h"
+
 #ifndef NF4_WAIT_LIMIT_NS
 // A bounded wait gives up after this long (nanoseconds of %globaltimer).
 #define NF4_WAIT_LIMIT_NS 1000000000ull
@@ -74,18 +76,32 @@ static __constant__ float c_thr[16] = {
     __builtin_huge_valf(),
 };
 
-// Error word codes (first error wins; the host reports any nonzero word as a timeout).
-enum : uint32_t {
-    kErrTimeoutFull = 0x101,      // waiting for a loaded stage
-    kErrTimeoutEmpty = 0x102,     // waiting for a stage to be released
-    kErrTimeoutConverted = 0x103, // waiting for converted weights
-    kErrTimeoutAccum = 0x104,     // waiting for the accumulator
-    kErrTimeoutDrain = 0x105,     // waiting for copies in flight at exit
-};
-
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) {
     if (err) atomicCAS(err, 0u, code);
 }
+
+// Checked build.  With -DNF4_CHECKED every global access that is not a TMA
+// tensor copy first tests its index against the extent of the buffer it
+// addresses, both in units of the access.  An index outside [0, extent)
+// records kErrBounds and the access is skipped (a skipped load reads zero),
+// so an indexing mistake becomes a status instead of a fault.  TMA tensor
+// copies need no test: the hardware clips every box to its tensor map, whose
+// extents the host sets from the validated sizes.  In the normal build the
+// test is the constant true and compiles away.  The test switch
+// NF4_TEST_SHRINK_EXTENT tests against extent - 1 instead, so the last
+// element of every checked buffer reports while no access leaves its buffer.
+#if defined(NF4_CHECKED)
+__device__ __forceinline__ bool in_bounds(uint32_t* err, int64_t i, int64_t extent) {
+#if defined(NF4_TEST_SHRINK_EXTENT)
+    extent -= 1;
+#endif
+    if (i >= 0 && i < extent) return true;
+    record_error(err, kErrBounds);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(uint32_t*, int64_t, int64_t) { return true; }
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
@@ -147,8 +163,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
     return r;
 }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) { return pack2<kBF16>(lo, hi); }
 
 // A word of two 16-bit values of type DT -> the two fp32 values (exact).
 template <int DT>
@@ -252,12 +266,15 @@ __device__ __forceinline__ void store_out(void* y, int64_t i, float v) {
 }
 
 // Store 16 values of output column n, rows m_first .. m_first + 15 of a
-// row-major output with `ld` columns, rounded to DT (fp32: as they are).
-// One pointer advanced by a row per value; the row bound is checked once
-// for the whole run unless it ends past M.  (Indexing every element from
-// (m, n) cost the GEMM epilogues about half their time.)
+// row-major output [M, ld], rounded to DT (fp32: as they are); rows at or
+// past M are not stored (a run may start past M: it stores nothing).  One
+// pointer advanced by a row per value; the row bound is checked once for the
+// whole run unless it ends past M.  (Indexing every element from (m, n) cost
+// the GEMM epilogues about half their time.)
 template <int DT>
-__device__ __forceinline__ void store_col16(void* y, int64_t ld, int m_first, int M, int n, const float (&v)[16]) {
+__device__ __forceinline__ void store_col16(void* y, int64_t ld, int m_first, int M, int n, const float (&v)[16],
+                                            uint32_t* err) {
+    if (m_first < M && (!in_bounds(err, n, ld) || !in_bounds(err, m_first, M))) return;
     using E = typename std::conditional<DT == kF32, float, uint16_t>::type;
     E* p = static_cast<E*>(y) + static_cast<int64_t>(m_first) * ld + n;
     auto cvt = [](float x) -> E {
@@ -409,17 +426,6 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D[tmem] (+)= A[smem] . B[smem]^T, both K-major bf16, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation issued so far by this

@@ -204,6 +204,8 @@ struct TsArgs {
     int M, N, K;          // N: output columns (rows of one half of a gate/up pair)
     int kb_per_split;
     int m_tiles;
+    int64_t am_count;     // scales in absmax
+    int64_t ws_floats;    // fp32 values the workspace holds (split)
     uint32_t* err;
 };
 
@@ -328,7 +330,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int kb = kb0 + st * KS;
             produce_weights<C::BW, KS, GEGLU>(bar.pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(p_tile(p)),
                                                  kb * kPackedRow, n0, args.N + n0, args.N, smem_u32(am_tile(p)),
-                                                 args.absmax, nk_total, kb);
+                                                 args.absmax, nk_total, kb, args.am_count, args.err);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(bar.pfull(0), SP, issued, args.err);
@@ -545,7 +547,7 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                             const float other = xbuf[(c0 + i) * HW + rr];
                             o[i] = gate ? gelu_tanh(mine) * other : gelu_tanh(other) * mine;
                         }
-                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o);
+                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o, args.err);
                     }
                 }
             }
@@ -562,11 +564,13 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     float o[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[i]);
-                    if constexpr (SPLIT)   // this split's fp32 partial, [splits][M][N]
-                        store_col16<kF32>(args.ws + static_cast<int64_t>(split) * args.M * args.N, args.N, m0 + c0,
-                                          args.M, n, o);
-                    else
-                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o);
+                    if constexpr (SPLIT) {   // this split's fp32 partial, [splits][M][N]
+                        const int64_t plane = static_cast<int64_t>(args.M) * args.N;
+                        if (in_bounds(args.err, (split + 1) * plane - 1, args.ws_floats))
+                            store_col16<kF32>(args.ws + split * plane, args.N, m0 + c0, args.M, n, o, args.err);
+                    } else {
+                        store_col16<DT>(args.y, args.N, m0 + c0, args.M, n, o, args.err);
+                    }
                 }
             }
         }
@@ -583,16 +587,19 @@ ts_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     }
 }
 
-// Sum the split-K partials in split order and store once in DT.
+// Sum the split-K partials in split order and store once in DT.  ws holds
+// ws_floats values.
 template <int DT>
-__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn, void* __restrict__ y) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t mn, void* __restrict__ y,
+                                     int64_t ws_floats, uint32_t* err) {
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < mn;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float acc = ws[i];
-        for (int s = 1; s < splits; ++s) acc += ws[static_cast<int64_t>(s) * mn + i];
-        store_out<DT>(y, i, acc);
+        auto at = [&](int64_t j) { return in_bounds(err, j, ws_floats) ? ws[j] : 0.0f; };
+        float acc = at(i);
+        for (int s = 1; s < splits; ++s) acc += at(static_cast<int64_t>(s) * mn + i);
+        if (in_bounds(err, i, mn)) store_out<DT>(y, i, acc);
     }
 }
 
@@ -601,20 +608,22 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
 // write DT(gelu(gate) * up), [M, F].
 template <int DT>
 __global__ void splitk_geglu_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t F,
-                                           void* __restrict__ y) {
+                                           void* __restrict__ y, int64_t ws_floats, uint32_t* err) {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t mn2 = M * 2 * F;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * F;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t m = i / F, n = i - m * F;
-        const float* g = ws + m * 2 * F + n;
-        float gs = g[0], us = g[F];
+        const int64_t g0 = m * 2 * F + n;   // gate partial of split 0; the up partial is F further
+        const float* g = ws + g0;
+        auto at = [&](int64_t j) { return in_bounds(err, g0 + j, ws_floats) ? g[j] : 0.0f; };
+        float gs = at(0), us = at(F);
         for (int s = 1; s < splits; ++s) {
-            gs += g[s * mn2];
-            us += g[s * mn2 + F];
+            gs += at(s * mn2);
+            us += at(s * mn2 + F);
         }
-        store_out<DT>(y, i, gelu_tanh(gs) * us);
+        if (in_bounds(err, i, M * F)) store_out<DT>(y, i, gelu_tanh(gs) * us);
     }
 }
 
@@ -778,7 +787,7 @@ cudaError_t dispatch_nx(const DeviceInfo& dev, const Plan& p, const CUtensorMap&
 template <int DT>
 cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const void* x, int64_t M, int64_t K,
                         const uint8_t* packed, const float* absmax, int64_t N, void* y, float* ws,
-                        cudaStream_t s) {
+                        int64_t ws_floats, cudaStream_t s) {
     if (pair && (p.split || N % 2 != 0)) return cudaErrorInvalidValue;
     CUtensorMap tm_x, tm_w;
     constexpr bool F32 = DT == kF32;
@@ -797,7 +806,7 @@ cudaError_t launch_plan(const DeviceInfo& dev, const Plan& p, bool pair, const v
                   kPackedRow * ks, wsw))
         return cudaErrorInvalidValue;
     TsArgs a{absmax, y, ws, static_cast<int>(M), static_cast<int>(pair ? N / 2 : N), static_cast<int>(K),
-             p.kb_per_split, p.m_tiles, dev.err_word};
+             p.kb_per_split, p.m_tiles, N * (K / kBlock), ws_floats, dev.err_word};
     if constexpr (F32) {
         if (p.split)
             return dispatch_nx<true, kKsSplitF32, kRsSplitF32, 0, false, DT>(dev, p, tm_x, tm_w, a, s);
@@ -830,7 +839,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t
     const Plan p = make_plan(M, N, K);
     if (p.split) return cudaErrorInvalidValue;
     return with_dt(dtype, [&](auto dt) {
-        return launch_plan<decltype(dt)::value>(dev, p, false, x, M, K, packed, absmax, N, y, nullptr, s);
+        return launch_plan<decltype(dt)::value>(dev, p, false, x, M, K, packed, absmax, N, y, nullptr, 0, s);
     });
 }
 
@@ -841,7 +850,7 @@ cudaError_t launch_gemm_geglu(const DeviceInfo& dev, int dtype, const void* x, i
     const Plan p = make_plan(M, 2 * F, K);
     if (p.split) return cudaErrorInvalidValue;
     return with_dt(dtype, [&](auto dt) {
-        return launch_plan<decltype(dt)::value>(dev, p, true, x, M, K, packed, absmax, 2 * F, y, nullptr, s);
+        return launch_plan<decltype(dt)::value>(dev, p, true, x, M, K, packed, absmax, 2 * F, y, nullptr, 0, s);
     });
 }
 
@@ -871,10 +880,11 @@ cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64
     const Plan p = make_plan(M, N, K);
     if (!p.split) return cudaErrorInvalidValue;
     workspace = static_cast<uint8_t*>(workspace) + gemv_header_bytes();   // the counters stay untouched
+    const int64_t ws_floats = static_cast<int64_t>((ws_bytes - gemv_header_bytes()) / sizeof(float));
     return with_dt(dtype, [&](auto dtc) {
         constexpr int DT = decltype(dtc)::value;
-        if (cudaError_t e =
-                launch_plan<DT>(dev, p, false, x, M, K, packed, absmax, N, y, static_cast<float*>(workspace), s);
+        if (cudaError_t e = launch_plan<DT>(dev, p, false, x, M, K, packed, absmax, N, y,
+                                            static_cast<float*>(workspace), ws_floats, s);
             e != cudaSuccess)
             return e;
         const int64_t mn = geglu ? M * (N / 2) : M * N;   // outputs
@@ -882,8 +892,10 @@ cudaError_t launch_skinny(const DeviceInfo& dev, int dtype, const void* x, int64
         const int grid =
             static_cast<int>(std::min<int64_t>((mn + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
         const float* wsf = static_cast<const float*>(workspace);
-        cudaError_t e = geglu ? launch_pdl(splitk_geglu_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, M, N / 2, y)
-                              : launch_pdl(splitk_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, mn, y);
+        cudaError_t e = geglu ? launch_pdl(splitk_geglu_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, M, N / 2,
+                                           y, ws_floats, dev.err_word)
+                              : launch_pdl(splitk_reduce_kernel<DT>, grid, threads, 0, s, wsf, p.splits, mn, y, ws_floats,
+                                           dev.err_word);
         if (e != cudaSuccess) return e;
         count_launches(1);
         return cudaGetLastError();

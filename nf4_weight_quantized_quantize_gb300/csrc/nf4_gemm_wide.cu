@@ -103,6 +103,7 @@ struct WdArgs {
     void* y;               // [M, N] ([M, F] for a gate/up pair)
     int M, N, K;           // N: output columns (F for a gate/up pair)
     int m_tiles;
+    int64_t am_count;      // scales in absmax
     uint32_t* err;
 };
 
@@ -342,7 +343,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             uint8_t* ptile = smem + C::OFF_P + p * C::P_SLOT;
             produce_weights<C::BW, kWdKs, GEGLU>(pfull(p), lane, C::P_BYTES, &tm_w, smem_u32(ptile),
                                                  kb * kPackedRow, n0, args.N + n0, args.N,
-                                                 smem_u32(ptile + C::P_BYTES), args.absmax, nk, kb);
+                                                 smem_u32(ptile + C::P_BYTES), args.absmax, nk, kb, args.am_count,
+                                                 args.err);
             ++issued;
         }
         if (*abort_flag && lane == 0) drain_ring(pfull(0), SP, issued, args.err);
@@ -519,7 +521,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                             const float other = xbuf[(16 * ci + i) * (C::BW / 2) + rr];
                             o[i] = gate ? gelu_tanh(mine) * other : gelu_tanh(other) * mine;
                         }
-                        store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o);
+                        store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o, args.err);
                     }
                 }
             }
@@ -534,7 +536,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     float o[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(v[i]);
-                    store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o);
+                    store_col16<DT>(args.y, args.N, col_row(ci, 0), args.M, n, o, args.err);
                 }
             }
         }
@@ -589,7 +591,8 @@ cudaError_t launch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int
     const int64_t ctas = 2 * static_cast<int64_t>(p.m_tiles) * p.n_pairs;
     if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int64_t n_out = GEGLU ? N / 2 : N;
-    WdArgs a{absmax, y, static_cast<int>(M), static_cast<int>(n_out), static_cast<int>(K), p.m_tiles, dev.err_word};
+    WdArgs a{absmax, y, static_cast<int>(M), static_cast<int>(n_out), static_cast<int>(K), p.m_tiles, N * (K / kBK),
+             dev.err_word};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(kWdThreads);

@@ -118,6 +118,8 @@ struct GvArgs {
     int n_out;             // output columns: N, or F for a pair
     int n_tiles, splits, kb_per_split;
     int scale_tma;         // the scales come by TMA (K % 256 == 0), else by 4-byte copies
+    int64_t part_floats;   // fp32 values the partials area holds
+    int counter_count;     // arrival counters in the header
     uint32_t* err;
 };
 
@@ -250,12 +252,14 @@ __device__ __forceinline__ void store_rows(const GvArgs& a, const float (&v)[NT]
         for (int e = 0; e < 2; ++e) {
             const int m = m0 + e;
             if (m >= a.M) continue;
+            const int64_t i = static_cast<int64_t>(m) * a.n_out + n_lo;
+            const int64_t count = static_cast<int64_t>(a.M) * a.n_out;
             if constexpr (PAIR) {
-                if (n_lo < a.n_out)
-                    store_out<DT>(a.y, static_cast<int64_t>(m) * a.n_out + n_lo, gelu_tanh(v[nt][e]) * v[nt][2 + e]);
+                if (n_lo < a.n_out && in_bounds(a.err, i, count))
+                    store_out<DT>(a.y, i, gelu_tanh(v[nt][e]) * v[nt][2 + e]);
             } else {
-                if (n_lo < a.n_out) store_out<DT>(a.y, static_cast<int64_t>(m) * a.n_out + n_lo, v[nt][e]);
-                if (n_lo + 8 < a.n_out) store_out<DT>(a.y, static_cast<int64_t>(m) * a.n_out + n_lo + 8, v[nt][2 + e]);
+                if (n_lo < a.n_out && in_bounds(a.err, i, count)) store_out<DT>(a.y, i, v[nt][e]);
+                if (n_lo + 8 < a.n_out && in_bounds(a.err, i + 8, count)) store_out<DT>(a.y, i + 8, v[nt][2 + e]);
             }
         }
     }
@@ -364,8 +368,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                         n = n0 + row;
                         in = n < a.rows;
                     }
-                    const float* src = a.absmax + (in ? static_cast<int64_t>(n) * nk_total + kb + h : 0);
-                    cp_async_4(smem_u32(st + C::OFF_AM + (row * BL + h) * 4), src);
+                    const int64_t src = in ? static_cast<int64_t>(n) * nk_total + kb + h : 0;
+                    if (in_bounds(a.err, src, static_cast<int64_t>(a.rows) * nk_total))
+                        cp_async_4(smem_u32(st + C::OFF_AM + (row * BL + h) * 4), a.absmax + src);
                 }
             }
             if (!a.scale_tma) cp_async_arrive_noinc(full(p));
@@ -515,23 +520,29 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     // ---------------- split K: publish this CTA's partial; the last CTA of the
     // tile to arrive sums all of them in split order and writes Y
     constexpr int kRgFloats = NT * 128;   // one row group's partial: NT x 32 lanes x 4
+    // partial of split s: float4 index part(s) / 4 + 32 nt of the partials area
     auto part = [&](int s) {
-        return a.partials + ((static_cast<int64_t>(tile) * a.splits + s) * C::RG + rg) * kRgFloats + lane * 4;
+        return ((static_cast<int64_t>(tile) * a.splits + s) * C::RG + rg) * kRgFloats + lane * 4;
     };
+    const int64_t part_f4 = a.part_floats / 4;
     if (owner) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float4*>(part(split) + nt * 128) = make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
+            if (in_bounds(a.err, part(split) / 4 + 32 * nt, part_f4))
+                *reinterpret_cast<float4*>(a.partials + part(split) + nt * 128) =
+                    make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
     }
     // The barrier orders every consumer's partial before thread 0's arrival,
     // whose acquire-release atomic publishes them (cumulatively) to the CTA
     // that arrives last and acquires the others' partials for it.
     consumers_sync();
     if (threadIdx.x == 0) {
-        uint32_t before;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(a.counters + tile) : "memory");
+        uint32_t before = 0;
+        if (in_bounds(a.err, tile, a.counter_count))
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(a.counters + tile) : "memory");
         const bool last = before == static_cast<uint32_t>(a.splits - 1);
-        if (last) a.counters[tile] = 0u;   // ready for the next call: nothing else touches it in this one
+        if (last && in_bounds(a.err, tile, a.counter_count))
+            a.counters[tile] = 0u;   // ready for the next call: nothing else touches it in this one
         *last_flag = last ? 1 : 0;
     }
     consumers_sync();
@@ -548,7 +559,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 if (s == split)
                     w4[i][nt] = make_float4(v[nt][0], v[nt][1], v[nt][2], v[nt][3]);
                 else if (s < a.splits)
-                    w4[i][nt] = ldg_cg_f4(part(s) + nt * 128);
+                    w4[i][nt] = in_bounds(a.err, part(s) / 4 + 32 * nt, part_f4) ? ldg_cg_f4(a.partials + part(s) + nt * 128)
+                                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
@@ -615,7 +627,7 @@ GvPlan make_gv_plan(int64_t M, int64_t rows, int64_t K) {
 template <int DT, int BL, int NT, bool PAIR>
 cudaError_t launch_gv(const DeviceInfo& dev, const GvPlan& p, const void* x, int64_t M, int64_t K,
                       const uint8_t* packed, const float* absmax, int64_t rows, void* y, void* workspace,
-                      cudaStream_t s) {
+                      size_t ws_bytes, cudaStream_t s) {
     using C = GvCfg<BL>;
     if (dev.smem_optin < C::SMEM) return cudaErrorInvalidConfiguration;
     auto kernel = gemv_kernel<DT, BL, NT, PAIR>;
@@ -648,6 +660,8 @@ cudaError_t launch_gv(const DeviceInfo& dev, const GvPlan& p, const void* x, int
              p.splits,
              p.kb_per_split,
              scale_tma ? 1 : 0,
+             static_cast<int64_t>((ws_bytes - kGvHeaderBytes) / sizeof(float)),
+             static_cast<int>(kGvHeaderBytes / sizeof(uint32_t)),
              dev.err_word};
     const unsigned grid = static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.splits);
     if (cudaError_t e = launch_pdl(kernel, dim3(grid), dim3(kGvThreads), C::SMEM, s, tm_x, tm_w, tm_am, a); e != cudaSuccess)
@@ -658,13 +672,14 @@ cudaError_t launch_gv(const DeviceInfo& dev, const GvPlan& p, const void* x, int
 
 template <int DT, bool PAIR>
 cudaError_t dispatch_gv(const DeviceInfo& dev, const GvPlan& p, const void* x, int64_t M, int64_t K,
-                        const uint8_t* packed, const float* absmax, int64_t rows, void* y, void* ws, cudaStream_t s) {
+                        const uint8_t* packed, const float* absmax, int64_t rows, void* y, void* ws, size_t ws_bytes,
+                        cudaStream_t s) {
     if (p.bl == 4)
-        return p.nt == 1 ? launch_gv<DT, 4, 1, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, s)
-                         : launch_gv<DT, 4, 2, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, s);
+        return p.nt == 1 ? launch_gv<DT, 4, 1, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, ws_bytes, s)
+                         : launch_gv<DT, 4, 2, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, ws_bytes, s);
     if (p.bl == 8)
-        return p.nt == 1 ? launch_gv<DT, 8, 1, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, s)
-                         : launch_gv<DT, 8, 2, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, s);
+        return p.nt == 1 ? launch_gv<DT, 8, 1, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, ws_bytes, s)
+                         : launch_gv<DT, 8, 2, PAIR>(dev, p, x, M, K, packed, absmax, rows, y, ws, ws_bytes, s);
     return cudaErrorInvalidValue;
 }
 
@@ -693,11 +708,11 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int dtype, const void* x, int64_t
         return cudaErrorInvalidValue;
     switch (dtype) {
         case kBF16:
-            return pair ? dispatch_gv<kBF16, true>(dev, p, x, M, K, packed, absmax, rows, y, workspace, s)
-                        : dispatch_gv<kBF16, false>(dev, p, x, M, K, packed, absmax, rows, y, workspace, s);
+            return pair ? dispatch_gv<kBF16, true>(dev, p, x, M, K, packed, absmax, rows, y, workspace, ws_bytes, s)
+                        : dispatch_gv<kBF16, false>(dev, p, x, M, K, packed, absmax, rows, y, workspace, ws_bytes, s);
         case kF16:
-            return pair ? dispatch_gv<kF16, true>(dev, p, x, M, K, packed, absmax, rows, y, workspace, s)
-                        : dispatch_gv<kF16, false>(dev, p, x, M, K, packed, absmax, rows, y, workspace, s);
+            return pair ? dispatch_gv<kF16, true>(dev, p, x, M, K, packed, absmax, rows, y, workspace, ws_bytes, s)
+                        : dispatch_gv<kF16, false>(dev, p, x, M, K, packed, absmax, rows, y, workspace, ws_bytes, s);
         default:
             return cudaErrorInvalidValue;
     }

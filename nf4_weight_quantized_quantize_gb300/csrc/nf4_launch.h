@@ -32,6 +32,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Error word codes (the first one recorded wins).  nf4_last_error reports a
+// 0x1xx word as a timeout and a 0x2xx word as an index out of bounds.
+enum : uint32_t {
+    kErrTimeoutFull = 0x101,      // waiting for a loaded stage
+    kErrTimeoutEmpty = 0x102,     // waiting for a stage to be released
+    kErrTimeoutConverted = 0x103, // waiting for converted weights
+    kErrTimeoutAccum = 0x104,     // waiting for the accumulator
+    kErrTimeoutDrain = 0x105,     // waiting for copies in flight at exit
+    kErrBounds = 0x201,           // checked build: an index outside its buffer
+};
+
 struct DeviceInfo {
     int ordinal = -1;
     int sm_count = 0;

@@ -196,11 +196,11 @@ constexpr int kQuantUnroll = 1;   // 16-byte words in flight per thread
 // warp owns the 16-byte word t of a 512-byte warp tile (4 blocks); 8 lanes
 // share a block and reduce its absmax with shuffles.  Finite bf16 and fp16
 // magnitudes order like their 15-bit patterns, so the absmax is an integer
-// max over (bits & 0x7fff).
+// max over (bits & 0x7fff).  nwords covers whole blocks of the numel values.
 template <int DT>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __restrict__ packed,
-                    float* __restrict__ absmax) {
+                    float* __restrict__ absmax, int64_t numel, uint32_t* err) {
     __shared__ float s_thr[16];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
     __syncthreads();
@@ -217,7 +217,8 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t word = ((t0 + u * nwarps) << 5) + lane;
-            v[u] = (t0 + u * nwarps < ntiles && word < nwords) ? ldg_nc_v4(w + word) : make_uint4(0, 0, 0, 0);
+            v[u] = (t0 + u * nwarps < ntiles && word < nwords && in_bounds(err, word, numel / 8)) ? ldg_nc_v4(w + word)
+                                                                                           : make_uint4(0, 0, 0, 0);
         }
     };
     uint4 v[kQuantUnroll], nv[kQuantUnroll];
@@ -234,8 +235,9 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
             if (t0 + u * nwarps < ntiles && word < nwords) {
-                packed[word] = quantize8_fast<DT>(v[u], m, s_thr);
-                if ((lane & 7) == 0) absmax[word >> 3] = am_of<DT>(m);
+                if (in_bounds(err, word, numel / 8)) packed[word] = quantize8_fast<DT>(v[u], m, s_thr);
+                if ((lane & 7) == 0 && in_bounds(err, word >> 3, (numel + kBlock - 1) / kBlock))
+                    absmax[word >> 3] = am_of<DT>(m);
             }
         }
     }
@@ -246,7 +248,7 @@ quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __res
 // share a block.  Finite fp32 magnitudes order like their 31-bit patterns.
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_vec_f32_kernel(const uint4* __restrict__ w, int64_t nwords, uint16_t* __restrict__ packed,
-                        float* __restrict__ absmax) {
+                        float* __restrict__ absmax, int64_t numel, uint32_t* err) {
     __shared__ float s_thr[16];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
     __syncthreads();
@@ -258,7 +260,8 @@ quantize_vec_f32_kernel(const uint4* __restrict__ w, int64_t nwords, uint16_t* _
     const int64_t ntiles = (nwords + 31) >> 5;
     auto load = [&](int64_t t) {
         const int64_t word = (t << 5) + lane;
-        return (t < ntiles && word < nwords) ? ldg_nc_v4(w + word) : make_uint4(0, 0, 0, 0);
+        return (t < ntiles && word < nwords && in_bounds(err, word, numel / 4)) ? ldg_nc_v4(w + word)
+                                                                                : make_uint4(0, 0, 0, 0);
     };
     uint4 nv = make_uint4(0, 0, 0, 0);
     if (warp < ntiles) nv = load(warp);
@@ -273,8 +276,8 @@ quantize_vec_f32_kernel(const uint4* __restrict__ w, int64_t nwords, uint16_t* _
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
         if (word < nwords) {
             const float am = __uint_as_float(m);
-            packed[word] = static_cast<uint16_t>(quantize4_f32_fast(v, am, s_thr));
-            if ((lane & 15) == 0) absmax[word >> 4] = am;
+            if (in_bounds(err, word, numel / 4)) packed[word] = static_cast<uint16_t>(quantize4_f32_fast(v, am, s_thr));
+            if ((lane & 15) == 0 && in_bounds(err, word >> 4, (numel + kBlock - 1) / kBlock)) absmax[word >> 4] = am;
         }
     }
 }
@@ -294,7 +297,7 @@ __device__ __forceinline__ float load_elem(const void* w, int64_t i) {
 template <int DT>
 __global__ void quantize_scalar_kernel(const void* __restrict__ w, int64_t numel, int64_t b0,
                                        int64_t b1, uint8_t* __restrict__ packed,
-                                       float* __restrict__ absmax) {
+                                       float* __restrict__ absmax, uint32_t* err) {
     __shared__ float s_thr[16];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
     __syncthreads();
@@ -304,11 +307,13 @@ __global__ void quantize_scalar_kernel(const void* __restrict__ w, int64_t numel
          b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t lo = b * kBlock;
         const int64_t hi = min(lo + kBlock, numel);
+        auto elem = [&](int64_t i) { return in_bounds(err, i, numel) ? load_elem<DT>(w, i) : 0.0f; };
         float am = 0.0f;
-        for (int64_t i = lo; i < hi; ++i) am = fmaxf(am, fabsf(load_elem<DT>(w, i)));
-        absmax[b] = am;
+        for (int64_t i = lo; i < hi; ++i) am = fmaxf(am, fabsf(elem(i)));
+        if (in_bounds(err, b, (numel + kBlock - 1) / kBlock)) absmax[b] = am;
         for (int64_t i = lo; i < hi; i += 2)
-            packed[i >> 1] = static_cast<uint8_t>(code_byte_exact(load_elem<DT>(w, i), load_elem<DT>(w, i + 1), am, s_thr));
+            if (in_bounds(err, i >> 1, numel / 2))
+                packed[i >> 1] = static_cast<uint8_t>(code_byte_exact(elem(i), elem(i + 1), am, s_thr));
     }
 }
 
@@ -328,7 +333,7 @@ constexpr int kDequantTiles = 2;
 template <int DT>
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict__ absmax,
-                   int64_t ntiles, uint4* __restrict__ out) {
+                   int64_t ntiles, uint4* __restrict__ out, int64_t numel, uint32_t* err) {
     __shared__ uint32_t lut[256];
     for (int e = threadIdx.x; e < 256; e += kDequantThreads) lut[e] = lut_entry<DT>(static_cast<uint32_t>(e));
     __syncthreads();
@@ -346,8 +351,9 @@ dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict_
             const int64_t tile = min(t0 + u, ntiles - 1);   // past the end: reload the last tile, store nothing
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                p[4 * u + i] = ldg_nc_u32(packed + tile * 128 + 32 * i + lane);
-                a[4 * u + i] = ldg_nc_f32(absmax + tile * 16 + 4 * i + (lane >> 3));
+                const int64_t pi = tile * 128 + 32 * i + lane, ai = tile * 16 + 4 * i + (lane >> 3);
+                p[4 * u + i] = in_bounds(err, pi, numel / 8) ? ldg_nc_u32(packed + pi) : 0u;
+                a[4 * u + i] = in_bounds(err, ai, (numel + kBlock - 1) / kBlock) ? ldg_nc_f32(absmax + ai) : 0.0f;
             }
         }
 #pragma unroll
@@ -363,7 +369,7 @@ dequant_vec_kernel(const uint32_t* __restrict__ packed, const float* __restrict_
                     o.y = scale_entry<DT>(lut[(q >> 8) & 0xffu], am);
                     o.z = scale_entry<DT>(lut[(q >> 16) & 0xffu], am);
                     o.w = scale_entry<DT>(lut[q >> 24], am);
-                    stg_v4(out + tile * 128 + 32 * i + lane, o);
+                    if (in_bounds(err, tile * 128 + 32 * i + lane, numel / 8)) stg_v4(out + tile * 128 + 32 * i + lane, o);
                 }
             }
         }
@@ -379,7 +385,7 @@ constexpr int kDequantTilesF32 = 4;
 
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_vec_f32_kernel(const uint16_t* __restrict__ packed, const float* __restrict__ absmax,
-                       int64_t ntiles, uint4* __restrict__ out) {
+                       int64_t ntiles, uint4* __restrict__ out, int64_t numel, uint32_t* err) {
     __shared__ float code[16];
     if (threadIdx.x < 16) code[threadIdx.x] = c_code[threadIdx.x];
     __syncthreads();
@@ -397,8 +403,9 @@ dequant_vec_f32_kernel(const uint16_t* __restrict__ packed, const float* __restr
             const int64_t tile = min(t0 + u, ntiles - 1);   // past the end: reload the last tile, store nothing
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                p[2 * u + i] = packed[tile * 64 + 32 * i + lane];
-                a[2 * u + i] = ldg_nc_f32(absmax + tile * 4 + 2 * i + (lane >> 4));
+                const int64_t pi = tile * 64 + 32 * i + lane, ai = tile * 4 + 2 * i + (lane >> 4);
+                p[2 * u + i] = in_bounds(err, pi, numel / 4) ? packed[pi] : 0u;
+                a[2 * u + i] = in_bounds(err, ai, (numel + kBlock - 1) / kBlock) ? ldg_nc_f32(absmax + ai) : 0.0f;
             }
         }
 #pragma unroll
@@ -414,7 +421,7 @@ dequant_vec_f32_kernel(const uint16_t* __restrict__ packed, const float* __restr
                     o.y = __float_as_uint(code[q & 15u] * am);
                     o.z = __float_as_uint(code[(q >> 12) & 15u] * am);
                     o.w = __float_as_uint(code[(q >> 8) & 15u] * am);
-                    stg_v4(out + tile * 64 + 32 * i + lane, o);
+                    if (in_bounds(err, tile * 64 + 32 * i + lane, numel / 4)) stg_v4(out + tile * 64 + 32 * i + lane, o);
                 }
             }
         }
@@ -427,7 +434,7 @@ dequant_vec_f32_kernel(const uint16_t* __restrict__ packed, const float* __restr
 template <int DT>
 __global__ void dequant_scalar_kernel(const uint8_t* __restrict__ packed,
                                       const float* __restrict__ absmax, int64_t j0, int64_t j1,
-                                      void* __restrict__ out) {
+                                      void* __restrict__ out, int64_t numel, uint32_t* err) {
     __shared__ uint32_t lut[256];
     if constexpr (DT != kF32) {
         for (int e = threadIdx.x; e < 256; e += blockDim.x) lut[e] = lut_entry<DT>(static_cast<uint32_t>(e));
@@ -437,8 +444,9 @@ __global__ void dequant_scalar_kernel(const uint8_t* __restrict__ packed,
     pdl_launch_dependents();
     for (int64_t j = j0 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; j < j1;
          j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (!in_bounds(err, j, numel / 2) || !in_bounds(err, 2 * j + 1, numel)) continue;
         const uint32_t b = packed[j];
-        const float am = absmax[(2 * j) / kBlock];
+        const float am = in_bounds(err, (2 * j) / kBlock, (numel + kBlock - 1) / kBlock) ? absmax[(2 * j) / kBlock] : 0.0f;
         if constexpr (DT == kF32) {
             float* o = static_cast<float*>(out);
             o[2 * j] = c_code[b >> 4] * am;
@@ -486,12 +494,12 @@ cudaError_t launch_quantize_t(const DeviceInfo& dev, const void* w, int64_t nume
             const int grid = grid_for(dev, reinterpret_cast<const void*>(quantize_vec_f32_kernel), kQuantThreads,
                                       (ntiles + warps_per_cta - 1) / warps_per_cta);
             e = launch_pdl(quantize_vec_f32_kernel, grid, kQuantThreads, 0, s, static_cast<const uint4*>(w), nwords,
-                           reinterpret_cast<uint16_t*>(packed), absmax);
+                           reinterpret_cast<uint16_t*>(packed), absmax, numel, dev.err_word);
         } else {
             const int grid = grid_for(dev, reinterpret_cast<const void*>(quantize_vec_kernel<DT>), kQuantThreads,
                                       (ntiles + warps_per_cta - 1) / warps_per_cta);
             e = launch_pdl(quantize_vec_kernel<DT>, grid, kQuantThreads, 0, s, static_cast<const uint4*>(w), nwords,
-                           reinterpret_cast<uint32_t*>(packed), absmax);
+                           reinterpret_cast<uint32_t*>(packed), absmax, numel, dev.err_word);
         }
         if (e != cudaSuccess) return e;
         count_launches(1);
@@ -501,7 +509,8 @@ cudaError_t launch_quantize_t(const DeviceInfo& dev, const void* w, int64_t nume
         const int64_t n = nblocks - scalar_from;
         const int threads = 128;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 4 * static_cast<int64_t>(dev.sm_count)));
-        e = launch_pdl(quantize_scalar_kernel<DT>, grid, threads, 0, s, w, numel, scalar_from, nblocks, packed, absmax);
+        e = launch_pdl(quantize_scalar_kernel<DT>, grid, threads, 0, s, w, numel, scalar_from, nblocks, packed, absmax,
+                       dev.err_word);
         if (e != cudaSuccess) return e;
         count_launches(1);
     }
@@ -530,12 +539,14 @@ cudaError_t launch_dequantize_t(const DeviceInfo& dev, const uint8_t* packed, co
                 const int grid = grid_for(dev, reinterpret_cast<const void*>(dequant_vec_f32_kernel), kDequantThreads,
                                           items, 2);
                 e = launch_pdl(dequant_vec_f32_kernel, grid, kDequantThreads, 0, s,
-                               reinterpret_cast<const uint16_t*>(packed), absmax, ntiles, static_cast<uint4*>(out));
+                               reinterpret_cast<const uint16_t*>(packed), absmax, ntiles, static_cast<uint4*>(out), numel,
+                               dev.err_word);
             } else {
                 const int grid = grid_for(dev, reinterpret_cast<const void*>(dequant_vec_kernel<DT>), kDequantThreads,
                                           items, 2);
                 e = launch_pdl(dequant_vec_kernel<DT>, grid, kDequantThreads, 0, s,
-                               reinterpret_cast<const uint32_t*>(packed), absmax, ntiles, static_cast<uint4*>(out));
+                               reinterpret_cast<const uint32_t*>(packed), absmax, ntiles, static_cast<uint4*>(out), numel,
+                               dev.err_word);
             }
             if (e != cudaSuccess) return e;
             count_launches(1);
@@ -546,7 +557,8 @@ cudaError_t launch_dequantize_t(const DeviceInfo& dev, const uint8_t* packed, co
         const int64_t n = nbytes - scalar_from;
         const int threads = 256;
         const int grid = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 8 * static_cast<int64_t>(dev.sm_count)));
-        e = launch_pdl(dequant_scalar_kernel<DT>, grid, threads, 0, s, packed, absmax, scalar_from, nbytes, out);
+        e = launch_pdl(dequant_scalar_kernel<DT>, grid, threads, 0, s, packed, absmax, scalar_from, nbytes, out, numel,
+                       dev.err_word);
         if (e != cudaSuccess) return e;
         count_launches(1);
     }

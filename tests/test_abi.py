@@ -48,7 +48,8 @@ def test_library_links_no_torch_and_no_libcuda():
 def test_status_strings_and_version():
     for code, name in [(0, "NF4_OK"), (1, "NF4_ERR_NULL"), (2, "NF4_ERR_SHAPE"), (3, "NF4_ERR_ALIGN"),
                        (4, "NF4_ERR_BLOCKSIZE"), (5, "NF4_ERR_WORKSPACE"), (6, "NF4_ERR_DEVICE"),
-                       (7, "NF4_ERR_CUDA"), (8, "NF4_ERR_TIMEOUT"), (9, "NF4_ERR_DTYPE")]:
+                       (7, "NF4_ERR_CUDA"), (8, "NF4_ERR_TIMEOUT"), (9, "NF4_ERR_DTYPE"),
+                       (10, "NF4_ERR_BOUNDS")]:
         assert nf4.nf4_status_string(code) == name
     assert nf4.nf4_status_string(99) == "NF4_ERR_UNKNOWN"
     assert nf4.nf4_version() >= 100
@@ -202,3 +203,13 @@ def test_kernel_hash_ignores_comments_and_layout():
     assert bench.code_tokens(a) == bench.code_tokens(b) == "int f(int x) { return x + 1; }"
     assert bench.code_tokens(a) != bench.code_tokens(a.replace("x + 1", "x + 2"))
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_checked_build_loads_and_exports_every_symbol():
+    """The bounds-checked build (-DNF4_CHECKED) compiles for sm_103a, loads
+    without a GPU and exports the same entry points."""
+    lib = nf4.load_library(nf4_build.build(extra=nf4_build.CHECKED_FLAGS, out=nf4_build.CHECKED_LIB))
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.nf4_status_string(nf4.NF4_ERR_BOUNDS) == b"NF4_ERR_BOUNDS"
+    assert lib.nf4_quantize(FAKE, 127, 64, FAKE, FAKE, None) == nf4.NF4_ERR_SHAPE   # same host checks
