@@ -112,7 +112,7 @@ typedef enum nf4_dtype {
  *   packed  [numel / 2] bytes out
  *   absmax  [ceil(numel / 64)] fp32 out
  *
- * Alignment: none required; 16-byte aligned w and 4-byte aligned packed take
+ * Alignment: none required; 16-byte aligned w and 8-byte aligned packed take
  * the vectorized kernel, anything else a slower element-wise kernel with
  * identical results.  Results are bit-exact: one correct answer exists.
  * Inputs must be finite (NaN/Inf give unspecified codes).

@@ -55,26 +55,33 @@ __device__ __forceinline__ uint32_t quantize8(uint4 v, uint32_t am_bits, const f
 // Fast code selection.  n = w / absmax is approximated by q = w * rcp(absmax)
 // with a correctly rounded reciprocal: |q - n| <= 3 * 2^-24 * |n| <= 2^-22.
 //
-// A degree-5 polynomial h, fitted to h(T_j) ~ j at the 15 thresholds and
-// monotone on [-1, 1], gives est = round(h(q)) with est in {code - 1, code}
-// for every fp32 q in [-1 - 4 ulp, 1 + 4 ulp] (the true code of q is the
-// number of thresholds below q).  That was checked for all 2.1e9 such q; h
-// stays at least 0.032 away from the rounding boundaries that would break
-// it, far above fp32 evaluation error.  So one comparison with T[est] (T[15]
-// = +inf) decides the code of q: code = est + (q > T[est]).  The codes of q
-// and n can only differ if a threshold lies between them, and the only
-// threshold near q is T[est]; such words (|q - T[est]| <= 2^-21, a few per
-// hundred thousand) are redone on the exact path.  The rounding to an
-// integer rides on the last FMA: adding 1.5 * 2^23 leaves round(h) in the
-// low mantissa bits, so the constant term (7) is kept an integer.
-constexpr float kH5 = 1.6238466501235962f;
-constexpr float kH4 = 1.0259608030319214f;
-constexpr float kH3 = -5.9369730949401855f;
-constexpr float kH2 = -0.9115704298019409f;
-constexpr float kH1 = 11.66257095336914f;
-constexpr float kH0Magic = 12582919.0f;          // 7 + 1.5 * 2^23, exact in fp32
-constexpr int kMagicBits = 0x4B400000;           // bits of 1.5 * 2^23
-constexpr float kGuard = 0x1p-21f;
+// Cell table: q falls in cell c = round(16 q + 16), 0 .. 32 for |q| <= 1 +
+// a few ulps -- the fp32 sum 16 q + (16 + 1.5 * 2^23) rounds once, to the
+// integer c in the low mantissa bits (16 q is exact).  Cells are 1/16 wide
+// and neighbouring thresholds at least 0.08 apart, so the threshold T_k
+// nearest a cell's centre is the only one within 0.02 of any q in the cell,
+// and T_(k-1) < q < T_(k+1) there: the code of q is k + (q > T_k).  Entry c
+// is T_k with its low four fraction bits replaced by k + 1 (T_k moves by less
+// than 16 ulp, at most 2^-20).  So code = (bits(e) & 15) - 1 + (q > e), the
+// comparison made against the stored value.  It decides the code of q
+// correctly, and the code of n too, whenever |q - e| > 2^-19: then q is more
+// than 2^-20 from T_k and from every other threshold, farther than n is from
+// q.  Words with a quotient within 2^-19 of its entry (about one in 10^4)
+// are redone on the exact path.  The index is masked to the 64-entry table,
+// so even a non-finite weight (outside the contract) reads inside it.
+constexpr float kCellMagic = 12582928.0f;   // 16 + 1.5 * 2^23, exact in fp32
+constexpr float kGuard = 0x1p-19f;
+static __constant__ uint32_t c_cell[64] = {
+    0xbf591cd1u, 0xbf591cd1u, 0xbf591cd1u, 0xbf591cd1u, 0xbf591cd1u, 0xbf1c5272u, 0xbf1c5272u, 0xbf1c5272u,
+    0xbeeb8483u, 0xbeeb8483u, 0xbeadea74u, 0xbeadea74u, 0xbe703ce5u, 0xbe703ce5u, 0xbe0d38b6u, 0xbd3a7877u,
+    0x3d22faf8u, 0x3d22faf8u, 0x3df64869u, 0x3e5067eau, 0x3e9582dbu, 0x3e9582dbu, 0x3ec753fcu, 0x3ec753fcu,
+    0x3f006d0du, 0x3f006d0du, 0x3f248daeu, 0x3f248daeu, 0x3f248daeu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu,
+    0x3f5c89dfu,   // cells 33 .. 63 are never hit by a finite quotient; they repeat cell 32
+    0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu,
+    0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu,
+    0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu,
+    0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu, 0x3f5c89dfu,
+};
 
 // Two fp32 lanes in one 64-bit register pair, for the packed f32x2 ops
 // (each lane rounds exactly like the scalar op).
@@ -97,17 +104,13 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// Code of one quotient q given h(q) + 1.5 * 2^23 in `hm`.  For |q| <= 1 + 8
-// ulp the estimate round(h(q)) is bits(hm) - bits(1.5 * 2^23), 0 .. 15; the
-// magic's low four bits are zero, so that equals bits(hm) & 15 -- which keeps
-// the table index in range whatever q is (a non-finite input gives an
-// unspecified code, never an out-of-range read).
-__device__ __forceinline__ uint32_t code_from_estimate(float q, float hm, const float* s_thr, bool& exact_needed) {
-    static_assert((kMagicBits & 15) == 0, "the estimate is the low bits of the rounded sum");
-    const uint32_t est = __float_as_uint(hm) & 15u;
-    const float t = s_thr[est];
-    exact_needed |= !(fabsf(q - t) > kGuard);
-    return est + (q > t ? 1u : 0u);
+// Code of one quotient q from its cell value cm = 16 q + 16 + 1.5 * 2^23 (the
+// cell index in the low bits); dmin keeps the smallest |q - entry| seen.
+__device__ __forceinline__ uint32_t code_from_cell(float q, float cm, const uint32_t* s_cell, float& dmin) {
+    const uint32_t e = s_cell[__float_as_uint(cm) & 63u];
+    const float d = q - __uint_as_float(e);
+    dmin = fminf(dmin, fabsf(d));
+    return (e & 15u) - (d > 0.0f ? 0u : 1u);
 }
 
 // Below the smallest normal fp32 the reciprocal of an absmax can overflow:
@@ -115,62 +118,83 @@ __device__ __forceinline__ uint32_t code_from_estimate(float q, float hm, const 
 constexpr float kMinNormal = 0x1p-126f;
 
 // The packed byte of two values (w0 in the high nibble): the quotients and
-// the polynomial run as f32x2 pairs.
-__device__ __forceinline__ uint32_t code_pair(float w0, float w1, uint64_t rcp2, const float* s_thr, bool& exact_needed) {
+// their cells run as f32x2 pairs.
+__device__ __forceinline__ uint32_t code_pair(float w0, float w1, uint64_t rcp2, const uint32_t* s_cell, float& dmin) {
     const uint64_t q2 = mul_f32x2(pack_f32x2(w0, w1), rcp2);
-    uint64_t h2 = fma_f32x2(pack_f32x2(kH5, kH5), q2, pack_f32x2(kH4, kH4));
-    h2 = fma_f32x2(h2, q2, pack_f32x2(kH3, kH3));
-    h2 = fma_f32x2(h2, q2, pack_f32x2(kH2, kH2));
-    h2 = fma_f32x2(h2, q2, pack_f32x2(kH1, kH1));
-    h2 = fma_f32x2(h2, q2, pack_f32x2(kH0Magic, kH0Magic));
-    float q0, q1, h0, h1;
+    const uint64_t c2 = fma_f32x2(q2, pack_f32x2(16.0f, 16.0f), pack_f32x2(kCellMagic, kCellMagic));
+    float q0, q1, c0, c1;
     unpack_f32x2(q2, q0, q1);
-    unpack_f32x2(h2, h0, h1);
-    const uint32_t c0 = code_from_estimate(q0, h0, s_thr, exact_needed);
-    const uint32_t c1 = code_from_estimate(q1, h1, s_thr, exact_needed);
-    return (c0 << 4) | c1;   // element 2i in the high nibble
+    unpack_f32x2(c2, c0, c1);
+    const uint32_t k0 = code_from_cell(q0, c0, s_cell, dmin);
+    const uint32_t k1 = code_from_cell(q1, c1, s_cell, dmin);
+    return (k0 << 4) | k1;   // element 2i in the high nibble
 }
 
 // The packed byte of one word of two 16-bit values of type DT.
 template <int DT>
-__device__ __forceinline__ uint32_t code_pair16(uint32_t word, uint64_t rcp2, const float* s_thr, bool& exact_needed) {
+__device__ __forceinline__ uint32_t code_pair16(uint32_t word, uint64_t rcp2, const uint32_t* s_cell, float& dmin) {
     const float2 w = unpack2<DT>(word);
-    return code_pair(w.x, w.y, rcp2, s_thr, exact_needed);
+    return code_pair(w.x, w.y, rcp2, s_cell, dmin);
 }
 
-// quantize8 with the fast path: one reciprocal per block, the exact path only
-// for words the estimate cannot decide.
+// The 4 packed bytes of one word of 8 16-bit values of type DT (the first
+// value in the high nibble of the lowest byte), by the cell table.
 template <int DT>
-__device__ __forceinline__ uint32_t quantize8_fast(uint4 v, uint32_t am_bits, const float* s_thr) {
-    if (am_bits == 0u) return 0x77777777u;
+__device__ __forceinline__ uint32_t codes8(uint4 v, uint64_t rcp2, const uint32_t* s_cell, float& dmin) {
+    return code_pair16<DT>(v.x, rcp2, s_cell, dmin) | (code_pair16<DT>(v.y, rcp2, s_cell, dmin) << 8) |
+           (code_pair16<DT>(v.z, rcp2, s_cell, dmin) << 16) | (code_pair16<DT>(v.w, rcp2, s_cell, dmin) << 24);
+}
+
+// Two consecutive words of one block (16 values) against its absmax pattern
+// `am_bits`: one reciprocal, the cell table, and the exact path for both
+// words if any quotient lies within the guard of its entry.
+template <int DT>
+__device__ __forceinline__ uint2 quantize16_fast(uint4 a, uint4 b, uint32_t am_bits, const float* s_thr,
+                                                 const uint32_t* s_cell) {
+    if (am_bits == 0u) return make_uint2(0x77777777u, 0x77777777u);
     const float am = am_of<DT>(am_bits);
     const float rcp = __frcp_rn(am);
     const uint64_t rcp2 = pack_f32x2(rcp, rcp);
-    // a subnormal absmax: the reciprocal may be infinite, the estimates then
-    // unspecified (but in range) -- take the exact path for the whole word
-    bool exact_needed = am < kMinNormal;
-    const uint32_t out = code_pair16<DT>(v.x, rcp2, s_thr, exact_needed) |
-                         (code_pair16<DT>(v.y, rcp2, s_thr, exact_needed) << 8) |
-                         (code_pair16<DT>(v.z, rcp2, s_thr, exact_needed) << 16) |
-                         (code_pair16<DT>(v.w, rcp2, s_thr, exact_needed) << 24);
-    return exact_needed ? quantize8<DT>(v, am_bits, s_thr) : out;
+    // a subnormal absmax: the reciprocal may be infinite, the codes then
+    // unspecified (but in range) -- take the exact path
+    float dmin = am < kMinNormal ? 0.0f : __int_as_float(0x7f800000);
+    const uint2 out = make_uint2(codes8<DT>(a, rcp2, s_cell, dmin), codes8<DT>(b, rcp2, s_cell, dmin));
+    if (dmin > kGuard) return out;
+    return make_uint2(quantize8<DT>(a, am_bits, s_thr), quantize8<DT>(b, am_bits, s_thr));
 }
 
-// Four fp32 values (one 16-byte word) against a block absmax -> 2 packed
-// bytes (the first in the low byte), fast path with the exact fallback.
-__device__ __forceinline__ uint32_t quantize4_f32_fast(uint4 v, float am, const float* s_thr) {
-    if (am == 0.0f) return 0x7777u;
-    if (am < kMinNormal)   // as in quantize8_fast; an early exit keeps this kernel within 32 registers
-        return code_byte_exact(__uint_as_float(v.x), __uint_as_float(v.y), am, s_thr) |
-               (code_byte_exact(__uint_as_float(v.z), __uint_as_float(v.w), am, s_thr) << 8);
-    const float rcp = __frcp_rn(am);
-    const uint64_t rcp2 = pack_f32x2(rcp, rcp);
-    bool exact_needed = false;
-    const float w0 = __uint_as_float(v.x), w1 = __uint_as_float(v.y);
-    const float w2 = __uint_as_float(v.z), w3 = __uint_as_float(v.w);
-    const uint32_t out = code_pair(w0, w1, rcp2, s_thr, exact_needed) | (code_pair(w2, w3, rcp2, s_thr, exact_needed) << 8);
-    if (!exact_needed) return out;
-    return code_byte_exact(w0, w1, am, s_thr) | (code_byte_exact(w2, w3, am, s_thr) << 8);
+// The 2 packed bytes of one word of 4 fp32 values (the first in the low
+// byte), by the cell table.
+__device__ __forceinline__ uint32_t codes4_f32(uint4 v, uint64_t rcp2, const uint32_t* s_cell, float& dmin) {
+    return code_pair(__uint_as_float(v.x), __uint_as_float(v.y), rcp2, s_cell, dmin) |
+           (code_pair(__uint_as_float(v.z), __uint_as_float(v.w), rcp2, s_cell, dmin) << 8);
+}
+
+// The same by exact division.
+__device__ __forceinline__ uint32_t codes4_f32_exact(uint4 v, float am, const float* s_thr) {
+    return code_byte_exact(__uint_as_float(v.x), __uint_as_float(v.y), am, s_thr) |
+           (code_byte_exact(__uint_as_float(v.z), __uint_as_float(v.w), am, s_thr) << 8);
+}
+
+// Four consecutive words of one fp32 block (16 values) against its absmax:
+// 8 packed bytes, one reciprocal, the cell table, and the exact path for all
+// four words if any quotient lies within the guard of its entry (or the
+// absmax is subnormal, where the reciprocal may overflow).
+__device__ __forceinline__ uint2 quantize16_f32_fast(const uint4 (&v)[4], float am, const float* s_thr,
+                                                     const uint32_t* s_cell) {
+    if (am == 0.0f) return make_uint2(0x77777777u, 0x77777777u);
+    float dmin = 0.0f;
+    uint2 out = make_uint2(0u, 0u);
+    if (am >= kMinNormal) {
+        const float rcp = __frcp_rn(am);
+        const uint64_t rcp2 = pack_f32x2(rcp, rcp);
+        dmin = __int_as_float(0x7f800000);
+        out.x = codes4_f32(v[0], rcp2, s_cell, dmin) | (codes4_f32(v[1], rcp2, s_cell, dmin) << 16);
+        out.y = codes4_f32(v[2], rcp2, s_cell, dmin) | (codes4_f32(v[3], rcp2, s_cell, dmin) << 16);
+    }
+    if (dmin > kGuard) return out;
+    return make_uint2(codes4_f32_exact(v[0], am, s_thr) | (codes4_f32_exact(v[1], am, s_thr) << 16),
+                      codes4_f32_exact(v[2], am, s_thr) | (codes4_f32_exact(v[3], am, s_thr) << 16));
 }
 
 // Per-halfword unsigned max of two words of 16-bit values.
@@ -180,104 +204,115 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// Largest 15-bit magnitude pattern among the 8 16-bit values of a 16-byte
-// word, reduced pairwise on both halves at once.  Finite bf16 and fp16
+// Largest 15-bit magnitude pattern among the 16 16-bit values of two 16-byte
+// words, reduced pairwise on both halves at once.  Finite bf16 and fp16
 // magnitudes both order like their 15-bit patterns.
-__device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
-    const uint32_t m2 = max_u16x2(max_u16x2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
-                                  max_u16x2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu));
+__device__ __forceinline__ uint32_t absmax_bits16(uint4 a, uint4 b) {
+    constexpr uint32_t M = 0x7fff7fffu;
+    const uint32_t m2 = max_u16x2(max_u16x2(max_u16x2(a.x & M, a.y & M), max_u16x2(a.z & M, a.w & M)),
+                                  max_u16x2(max_u16x2(b.x & M, b.y & M), max_u16x2(b.z & M, b.w & M)));
     return max(m2 & 0xffffu, m2 >> 16);
 }
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 1;   // 16-byte words in flight per thread
 
-// Vectorized quantizer for whole blocks of a 16-bit type DT.  Thread t of a
-// warp owns the 16-byte word t of a 512-byte warp tile (4 blocks); 8 lanes
-// share a block and reduce its absmax with shuffles.  Finite bf16 and fp16
-// magnitudes order like their 15-bit patterns, so the absmax is an integer
-// max over (bits & 0x7fff).  nwords covers whole blocks of the numel values.
+// Vectorized quantizer for whole blocks of a 16-bit type DT.  A warp tile is
+// 1 KB (8 blocks): lane t owns the 16-byte words 2t and 2t + 1, so 4 lanes
+// share a block, reduce its absmax with 2 shuffles and each takes one
+// reciprocal for its 16 values.  Finite bf16 and fp16 magnitudes order like
+// their 15-bit patterns, so the absmax is an integer max over (bits &
+// 0x7fff).  nwords (a multiple of 8) covers whole blocks of the numel values;
+// each lane writes its 8 packed bytes at once.
 template <int DT>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint32_t* __restrict__ packed,
+quantize_vec_kernel(const uint4* __restrict__ w, int64_t nwords, uint2* __restrict__ packed,
                     float* __restrict__ absmax, int64_t numel, uint32_t* err) {
     __shared__ float s_thr[16];
+    __shared__ uint32_t s_cell[64];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
+    if (threadIdx.x < 64) s_cell[threadIdx.x] = c_cell[threadIdx.x];
     __syncthreads();
     pdl_wait();                 // the previous kernel on the stream has finished
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kQuantThreads) >> 5;
-    const int64_t ntiles = (nwords + 31) >> 5;
-    // kQuantUnroll tiles per warp and iteration; the next iteration's words are
-    // loaded before this one's are converted, so each warp keeps a DRAM round
-    // trip in flight while it computes
-    auto load = [&](int64_t t0, uint4 (&v)[kQuantUnroll]) {
-#pragma unroll
-        for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t word = ((t0 + u * nwarps) << 5) + lane;
-            v[u] = (t0 + u * nwarps < ntiles && word < nwords && in_bounds(err, word, numel / 8)) ? ldg_nc_v4(w + word)
-                                                                                           : make_uint4(0, 0, 0, 0);
+    const int64_t npairs = nwords >> 1;          // word pairs; 4 per block
+    const int64_t ntiles = (npairs + 31) >> 5;
+    // the next tile's words are loaded before this one's are converted, so
+    // each warp keeps a DRAM round trip in flight while it computes
+    auto load = [&](int64_t t, uint4& a, uint4& b) {
+        const int64_t pr = (t << 5) + lane;
+        if (t < ntiles && pr < npairs && in_bounds(err, 2 * pr + 1, numel / 8)) {
+            a = ldg_nc_v4(w + 2 * pr);
+            b = ldg_nc_v4(w + 2 * pr + 1);
+        } else {
+            a = b = make_uint4(0, 0, 0, 0);
         }
     };
-    uint4 v[kQuantUnroll], nv[kQuantUnroll];
-    if (warp < ntiles) load(warp, nv);
-    for (int64_t t0 = warp; t0 < ntiles; t0 += nwarps * kQuantUnroll) {
-#pragma unroll
-        for (int u = 0; u < kQuantUnroll; ++u) v[u] = nv[u];
-        if (t0 + nwarps * kQuantUnroll < ntiles) load(t0 + nwarps * kQuantUnroll, nv);
-#pragma unroll
-        for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t word = ((t0 + u * nwarps) << 5) + lane;
-            uint32_t m = absmax_bits8(v[u]);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            if (t0 + u * nwarps < ntiles && word < nwords) {
-                if (in_bounds(err, word, numel / 8)) packed[word] = quantize8_fast<DT>(v[u], m, s_thr);
-                if ((lane & 7) == 0 && in_bounds(err, word >> 3, (numel + kBlock - 1) / kBlock))
-                    absmax[word >> 3] = am_of<DT>(m);
-            }
+    uint4 a, b, na, nb;
+    if (warp < ntiles) load(warp, na, nb);
+    for (int64_t t = warp; t < ntiles; t += nwarps) {
+        a = na;
+        b = nb;
+        if (t + nwarps < ntiles) load(t + nwarps, na, nb);
+        const int64_t pr = (t << 5) + lane;
+        uint32_t m = absmax_bits16(a, b);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (pr < npairs) {
+            if (in_bounds(err, pr, numel / 16)) packed[pr] = quantize16_fast<DT>(a, b, m, s_thr, s_cell);
+            if ((lane & 3) == 0 && in_bounds(err, pr >> 2, (numel + kBlock - 1) / kBlock))
+                absmax[pr >> 2] = am_of<DT>(m);
         }
     }
 }
 
-// Vectorized quantizer for whole blocks of fp32.  Thread t of a warp owns
-// the 16-byte word t (4 values) of a 512-byte warp tile (2 blocks); 16 lanes
-// share a block.  Finite fp32 magnitudes order like their 31-bit patterns.
+// Vectorized quantizer for whole blocks of fp32.  A warp tile is 2 KB (8
+// blocks): lane t owns the 16-byte words 4t .. 4t + 3 (16 values), so 4 lanes
+// share a block, reduce its absmax with 2 shuffles and each takes one
+// reciprocal for its 16 values.  Finite fp32 magnitudes order like their
+// 31-bit patterns.  nwords (a multiple of 16) covers whole blocks of the
+// numel values; each lane writes its 8 packed bytes at once.
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_vec_f32_kernel(const uint4* __restrict__ w, int64_t nwords, uint16_t* __restrict__ packed,
+quantize_vec_f32_kernel(const uint4* __restrict__ w, int64_t nwords, uint2* __restrict__ packed,
                         float* __restrict__ absmax, int64_t numel, uint32_t* err) {
     __shared__ float s_thr[16];
+    __shared__ uint32_t s_cell[64];
     if (threadIdx.x < 16) s_thr[threadIdx.x] = c_thr[threadIdx.x];
+    if (threadIdx.x < 64) s_cell[threadIdx.x] = c_cell[threadIdx.x];
     __syncthreads();
     pdl_wait();                 // the previous kernel on the stream has finished
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kQuantThreads) >> 5;
-    const int64_t ntiles = (nwords + 31) >> 5;
-    auto load = [&](int64_t t) {
-        const int64_t word = (t << 5) + lane;
-        return (t < ntiles && word < nwords && in_bounds(err, word, numel / 4)) ? ldg_nc_v4(w + word)
-                                                                                : make_uint4(0, 0, 0, 0);
+    const int64_t nquads = nwords >> 2;          // word quads; 4 per block
+    const int64_t ntiles = (nquads + 31) >> 5;
+    // the next tile's words are loaded before this one's are converted
+    auto load = [&](int64_t t, uint4 (&v)[4]) {
+        const int64_t qd = (t << 5) + lane;
+        const bool ok = t < ntiles && qd < nquads && in_bounds(err, 4 * qd + 3, numel / 4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = ok ? ldg_nc_v4(w + 4 * qd + i) : make_uint4(0, 0, 0, 0);
     };
-    uint4 nv = make_uint4(0, 0, 0, 0);
-    if (warp < ntiles) nv = load(warp);
+    uint4 v[4], nv[4];
+    if (warp < ntiles) load(warp, nv);
     for (int64_t t = warp; t < ntiles; t += nwarps) {
-        const uint4 v = nv;
-        if (t + nwarps < ntiles) nv = load(t + nwarps);   // next tile's word in flight meanwhile
-        const int64_t word = (t << 5) + lane;
-        uint32_t m = max(max(v.x & 0x7fffffffu, v.y & 0x7fffffffu), max(v.z & 0x7fffffffu, v.w & 0x7fffffffu));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = nv[i];
+        if (t + nwarps < ntiles) load(t + nwarps, nv);
+        const int64_t qd = (t << 5) + lane;
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            m = max(m, max(max(v[i].x & 0x7fffffffu, v[i].y & 0x7fffffffu), max(v[i].z & 0x7fffffffu, v[i].w & 0x7fffffffu)));
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        if (word < nwords) {
+        if (qd < nquads) {
             const float am = __uint_as_float(m);
-            if (in_bounds(err, word, numel / 4)) packed[word] = static_cast<uint16_t>(quantize4_f32_fast(v, am, s_thr));
-            if ((lane & 15) == 0 && in_bounds(err, word >> 4, (numel + kBlock - 1) / kBlock)) absmax[word >> 4] = am;
+            if (in_bounds(err, qd, numel / 16)) packed[qd] = quantize16_f32_fast(v, am, s_thr, s_cell);
+            if ((lane & 3) == 0 && in_bounds(err, qd >> 2, (numel + kBlock - 1) / kBlock)) absmax[qd >> 2] = am;
         }
     }
 }
@@ -477,29 +512,30 @@ namespace {
 template <int DT>
 cudaError_t launch_quantize_t(const DeviceInfo& dev, const void* w, int64_t numel, uint8_t* packed, float* absmax,
                               cudaStream_t s) {
-    constexpr int kElem = DT == kF32 ? 4 : 2;     // bytes per element
-    constexpr int kPerWord = 16 / kElem;          // elements per 16-byte word
+    constexpr int kPerWord = DT == kF32 ? 4 : 8;  // elements per 16-byte word
     cudaError_t e = cudaSuccess;
     const int64_t nblocks = (numel + kBlock - 1) / kBlock;
     const int64_t full = numel / kBlock;
+    // each lane of the vectorized kernels stores 8 packed bytes at once
     const bool aligned = (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
-                         (reinterpret_cast<uintptr_t>(packed) % (kPerWord / 2) == 0) &&
+                         (reinterpret_cast<uintptr_t>(packed) % 8 == 0) &&
                          (reinterpret_cast<uintptr_t>(absmax) % 4 == 0);
     int64_t scalar_from = 0;
     if (aligned && full > 0) {
         const int64_t nwords = full * (kBlock / kPerWord);
-        const int64_t ntiles = (nwords + 31) / 32;
+        // warp tiles: 128 words (32 quads) of fp32, 64 words (32 pairs) of a 16-bit type
+        const int64_t ntiles = DT == kF32 ? (nwords + 127) / 128 : (nwords + 63) / 64;
         const int64_t warps_per_cta = kQuantThreads / 32;
         if constexpr (DT == kF32) {
             const int grid = grid_for(dev, reinterpret_cast<const void*>(quantize_vec_f32_kernel), kQuantThreads,
                                       (ntiles + warps_per_cta - 1) / warps_per_cta);
             e = launch_pdl(quantize_vec_f32_kernel, grid, kQuantThreads, 0, s, static_cast<const uint4*>(w), nwords,
-                           reinterpret_cast<uint16_t*>(packed), absmax, numel, dev.err_word);
+                           reinterpret_cast<uint2*>(packed), absmax, numel, dev.err_word);
         } else {
             const int grid = grid_for(dev, reinterpret_cast<const void*>(quantize_vec_kernel<DT>), kQuantThreads,
                                       (ntiles + warps_per_cta - 1) / warps_per_cta);
             e = launch_pdl(quantize_vec_kernel<DT>, grid, kQuantThreads, 0, s, static_cast<const uint4*>(w), nwords,
-                           reinterpret_cast<uint32_t*>(packed), absmax, numel, dev.err_word);
+                           reinterpret_cast<uint2*>(packed), absmax, numel, dev.err_word);
         }
         if (e != cudaSuccess) return e;
         count_launches(1);

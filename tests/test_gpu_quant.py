@@ -124,6 +124,24 @@ def test_unaligned_pointers(offset):
     assert np.array_equal(workloads.bits(out), oracle.dequantize(p_ref, a_ref, n))
 
 
+@pytest.mark.parametrize("packed_offset", [4, 8])
+def test_packed_alignment_picks_the_kernel(packed_offset):
+    """The vectorized quantizer stores 8 packed bytes per lane: packed output
+    at a 4-byte (not 8-byte) boundary takes the element-wise kernel, at an
+    8-byte boundary the vectorized one; both are bit-exact."""
+    rs = np.random.default_rng(packed_offset)
+    n = 64 * 300
+    w = torch.from_numpy(rs.normal(0, 0.02, n).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    packed = torch.empty(n // 2 + 16, dtype=torch.uint8, device=DEV)[packed_offset:packed_offset + n // 2]
+    absmax = torch.empty(n // 64, dtype=torch.float32, device=DEV)
+    st = nf4.nf4_quantize(w.data_ptr(), n, 64, packed.data_ptr(), absmax.data_ptr(), 0)
+    assert st == nf4.NF4_OK
+    torch.cuda.synchronize()
+    p_ref, a_ref = oracle.quantize(workloads.bits(w))
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+    assert np.array_equal(absmax.cpu().numpy(), a_ref)
+
+
 def test_empty_is_a_no_op():
     assert nf4.nf4_quantize(0, 0, 64, 0, 0, 0) == nf4.NF4_OK
     assert nf4.nf4_dequantize(0, 0, 0, 64, 0, 0) == nf4.NF4_OK

@@ -1,17 +1,21 @@
-"""The quantizer's fast code estimate, checked on every fp32 quotient (CPU).
+"""The quantizer's fast code selection, checked on every fp32 quotient (CPU).
 
-nf4_quantize decides most codes from q = w * rcp(absmax) with a degree-5
-polynomial h: est = round(h(q)), then code = est + (q > T[est]).  That is
-right only if est is the code of q or one below it, for every fp32 q the
-kernel can see (|q| <= 1 + a few ulps).  This test reads the polynomial's
-constants from the CUDA source, takes the thresholds from the published
-codebook (tests/golden/nf4_codebook.txt, exact fp64 midpoints rounded down to
-fp32: the tie rule "nearest, ties to the lower index"), and walks all 2.1e9
-fp32 values in [-1 - 8 ulp, 1 + 8 ulp] in a small C program: h is evaluated
-in double precision and must stay at least 1e-3 inside the interval where
-rounding gives code - 1 or code, far more than the kernel's fp32 Horner
-error (< 1e-5 for |h| <= 16).  This is a check of the kernel's arithmetic
-from the kernel's own constants; the oracle is not involved.
+nf4_quantize decides most codes from q = w * rcp(absmax) through a cell table:
+cell c = round(16 q + 16) (the fp32 sum 16 q + 16 + 1.5 * 2^23, whose low
+mantissa bits hold c), entry e = table[c & 63] -- a threshold with its low four
+fraction bits replaced by its index + 1 -- and code = (bits(e) & 15) - 1 +
+(q > e).  The kernel takes that code only when |q - e| > guard and redoes the
+word by exact division otherwise.  This test reads the table, the cell
+constant and the guard from the CUDA source, takes the thresholds from the
+published codebook (tests/golden/nf4_codebook.txt, exact fp64 midpoints
+rounded down to fp32: the tie rule "nearest, ties to the lower index"), and
+walks all 2.1e9 fp32 values in [-1 - 8 ulp, 1 + 8 ulp] in a small C program,
+with the kernel's fp32 roundings.  Wherever the fast path is taken its code
+must be the code of q, and every threshold must be more than 2^-21 from q --
+farther than the exact quotient n = w / absmax can be from q (|q - n| <=
+3 * 2^-24 |n|), so n has the same code.  The cell index must stay in 0 .. 32.
+A check of the kernel's arithmetic from the kernel's own constants; the oracle
+is not involved.
 """
 import os
 import re
@@ -26,35 +30,40 @@ QUANT_CU = os.path.join(ROOT, "nf4_weight_quantized_quantize_gb300", "csrc", "nf
 CODEBOOK = os.path.join(ROOT, "tests", "golden", "nf4_codebook.txt")
 
 CHECKER = r"""
+#include <math.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 static float f_of(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+static uint32_t b_of(float f) { uint32_t b; memcpy(&b, &f, 4); return b; }
 int main(int argc, char** argv) {
     (void)argc;
-    double c[6]; float t[15];
-    for (int i = 0; i < 6; ++i) c[i] = (double)(float)strtod_wrap(argv[1 + i]);
-    for (int j = 0; j < 15; ++j) t[j] = (float)strtod_wrap(argv[7 + j]);
-    const double margin = 1e-3;
+    uint32_t cell[64]; float t[15];
+    const float magic = strtof(argv[1], 0), guard = strtof(argv[2], 0);
+    for (int i = 0; i < 64; ++i) cell[i] = (uint32_t)strtoul(argv[3 + i], 0, 0);
+    for (int j = 0; j < 15; ++j) t[j] = strtof(argv[67 + j], 0);
     const uint32_t hi = 0x3f800008u;   /* 1 + 8 ulp */
-    long long bad = 0, n = 0;
-    double worst = 1e9;
-    #pragma omp parallel for reduction(+:bad,n) reduction(min:worst) schedule(static)
+    long long n = 0, wrong = 0, near = 0, slow = 0, badidx = 0;
+    #pragma omp parallel for reduction(+:n,wrong,near,slow,badidx) schedule(static)
     for (long long k = 0; k <= 2LL * hi + 1; ++k) {
         const uint32_t b = (uint32_t)(k >> 1);
         const float q = (k & 1) ? -f_of(b) : f_of(b);
         int code = 0;
         for (int j = 0; j < 15; ++j) code += q > t[j];
-        const double x = (double)q;
-        const double h = ((((c[0] * x + c[1]) * x + c[2]) * x + c[3]) * x + c[4]) * x + c[5];
-        const double lo_gap = h - ((double)code - 1.5), hi_gap = ((double)code + 0.5) - h;
-        const double g = lo_gap < hi_gap ? lo_gap : hi_gap;
-        if (g < worst) worst = g;
-        /* round(h) must also index the 16-entry table */
-        if (g < margin || h < -0.5 + margin || h > 15.5 - margin) ++bad;
+        const float cm = q * 16.0f + magic;            /* 16 q exact, one rounding */
+        const uint32_t idx = b_of(cm) & 63u;
+        if (idx > 32u) ++badidx;
+        const uint32_t e = cell[idx];
+        const float d = q - f_of(e);
         ++n;
+        if (!(fabsf(d) > guard)) { ++slow; continue; }
+        const int fast = (int)(e & 15u) - (d > 0.0f ? 0 : 1);
+        if (fast != code) ++wrong;
+        for (int j = 0; j < 15; ++j)
+            if (fabs((double)q - (double)t[j]) <= 0x1p-21) ++near;
     }
-    printf("%lld %lld %.6f\n", n, bad, worst);
+    printf("%lld %lld %lld %lld %lld\n", n, wrong, near, slow, badidx);
     return 0;
 }
 """
@@ -62,15 +71,19 @@ int main(int argc, char** argv) {
 
 def kernel_constants():
     text = open(QUANT_CU).read()
-    vals = {}
-    for name in ("kH5", "kH4", "kH3", "kH2", "kH1", "kH0Magic"):
-        m = re.search(rf"constexpr float {name} = ([-0-9.eE+]+)f;", text)
-        assert m, f"{name} not found in nf4_quant.cu"
-        vals[name] = float(m.group(1))
-    magic = float(np.float32(1.5 * 2 ** 23))
-    c0 = float(np.float32(vals["kH0Magic"])) - magic
-    assert c0 == round(c0), "the constant term must be an integer so the rounding can ride on the last FMA"
-    return [vals["kH5"], vals["kH4"], vals["kH3"], vals["kH2"], vals["kH1"], c0]
+    m = re.search(r"constexpr float kCellMagic = ([0-9.]+)f;", text)
+    assert m, "kCellMagic not found in nf4_quant.cu"
+    magic = float(m.group(1))
+    assert magic == 16 + 1.5 * 2 ** 23
+    m = re.search(r"constexpr float kGuard = (0x1p-[0-9]+)f;", text)
+    assert m, "kGuard not found in nf4_quant.cu"
+    guard = float.fromhex(m.group(1))
+    m = re.search(r"c_cell\[64\] = \{(.*?)\};", text, flags=re.S)
+    assert m, "c_cell not found in nf4_quant.cu"
+    body = re.sub(r"//[^\n]*", "", m.group(1))
+    cells = [int(v, 16) for v in re.findall(r"0x([0-9a-fA-F]{8})u", body)]
+    assert len(cells) == 64
+    return magic, guard, cells
 
 
 def thresholds():
@@ -84,16 +97,35 @@ def thresholds():
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
-def test_estimate_is_code_or_one_below_for_every_fp32_quotient(tmp_path):
-    src = tmp_path / "est_check.c"
-    src.write_text("#include <stdlib.h>\nstatic double strtod_wrap(const char* s) { return strtod(s, 0); }\n"
-                   + CHECKER)
-    exe = tmp_path / "est_check"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", str(src), "-o", str(exe)],
-                   check=True)
-    args = [repr(float(np.float32(v))) for v in kernel_constants()] + [repr(v) for v in thresholds()]
+def test_cell_table_code_is_exact_for_every_fp32_quotient(tmp_path):
+    src = tmp_path / "cell_check.c"
+    src.write_text(CHECKER)
+    exe = tmp_path / "cell_check"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", str(src),
+                    "-o", str(exe), "-lm"], check=True)
+    magic, guard, cells = kernel_constants()
+    args = [repr(magic), repr(guard)] + [hex(c) for c in cells] + [repr(v) for v in thresholds()]
     out = subprocess.run([str(exe), *args], check=True, capture_output=True, text=True, timeout=600).stdout
-    n, bad, worst = out.split()
-    assert int(n) == 2 * (0x3F800008 + 1)
-    assert int(bad) == 0, f"{bad} quotients where round(h(q)) is not code or code - 1 (worst margin {worst})"
-    assert float(worst) > 1e-3
+    n, wrong, near, slow, badidx = (int(v) for v in out.split())
+    assert n == 2 * (0x3F800008 + 1)
+    assert badidx == 0, f"{badidx} quotients index past cell 32"
+    assert wrong == 0, f"{wrong} quotients where the fast path gives the wrong code"
+    assert near == 0, f"{near} fast-path quotients within 2^-21 of a threshold"
+    assert slow < n // 1000, f"{slow} quotients take the exact path"
+
+
+def test_cell_entries_carry_their_threshold():
+    """Each entry is a threshold T_k of the codebook, within 16 ulp, with k + 1
+    in its low four bits -- and the entries step through the thresholds in
+    order as the cells do."""
+    _, _, cells = kernel_constants()
+    t = np.array(thresholds(), dtype=np.float32)
+    ks = []
+    for e in cells[:33]:
+        k = (e & 15) - 1
+        assert 0 <= k < 15
+        tb = int(t[k].view(np.uint32))
+        assert abs(e - tb) < 16
+        ks.append(k)
+    assert ks == sorted(ks) and ks[0] == 0 and ks[-1] == 14
+    assert all(c == cells[32] for c in cells[33:])
