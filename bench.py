@@ -601,24 +601,28 @@ def _timed_mean(fn, stream, reps: int, flush):
     return statistics.mean(ts)
 
 
-def _skinny_stream(x, p, a, n, y, wsp, stream, calls: int = 64):
-    """Per-call time (ms) of back-to-back nf4_linear calls at a skinny batch,
-    the way a decode loop issues them: call i reads copy i % c of the weight,
-    with c copies holding more than three times the L2, so no call finds its
-    weight in L2.  The calls are captured once in a CUDA graph and replayed
-    between one pair of CUDA events, so the host's per-call launch work
-    (argument checks, tensor-map encoding) does not pace the device."""
+def _stream_per_call(x, p, a, n, y, wsp, stream, calls: int = 64, copy_x: bool = False):
+    """Per-call time (ms) of back-to-back nf4_linear calls, the way a model
+    issues them one after another: call i reads copy i % c of the weight (and,
+    with copy_x, of the activations), with c copies holding more than three
+    times the L2, so no call finds its inputs in L2.  The calls are captured
+    once in a CUDA graph and replayed between one pair of CUDA events, so
+    neither the host's per-call launch work (argument checks, tensor-map
+    encoding) nor the per-call events' own launch latency paces the device;
+    consecutive kernels overlap launch and prologue through programmatic
+    dependent launch, as they do in a model."""
     import torch
     import nf4_weight_quantized_quantize_gb300 as nf4
     l2 = getattr(torch.cuda.get_device_properties(x.device), "L2_cache_size", 128 << 20) or (128 << 20)
-    wbytes = p.numel() + 4 * a.numel()
+    wbytes = p.numel() + 4 * a.numel() + (x.numel() * x.element_size() if copy_x else 0)
     copies = max(2, -(-3 * l2 // wbytes))
     ps = [p.clone() for _ in range(copies)]
     am = [a.clone() for _ in range(copies)]
+    xs = [x.clone() for _ in range(copies)] if copy_x else [x] * copies
 
     def run():
         for i in range(calls):
-            nf4.linear(x, ps[i % copies], am[i % copies], n, out=y, workspace=wsp)
+            nf4.linear(xs[i % copies], ps[i % copies], am[i % copies], n, out=y, workspace=wsp)
 
     run()   # first calls on this device set up the library's per-device state
     torch.cuda.synchronize()
@@ -635,7 +639,7 @@ def _skinny_stream(x, p, a, n, y, wsp, stream, calls: int = 64):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / calls
-    del graph, ps, am
+    del graph, ps, am, xs
     return ms, copies, calls
 
 
@@ -645,8 +649,8 @@ def configs_block(dev, reps: int = 50):
     at its batch -- TFLOP/s against the bf16 peak for M >= 128, GB/s of the
     algorithmic bytes (0.5625 B per weight + X + Y) against the HBM peak for
     the skinny batches.  Mean of `reps` calls, L2 flushed before each; the
-    skinny batches of the large weights also as a stream of back-to-back
-    calls over distinct weight copies (`_skinny_stream`)."""
+    batches of the large weights also as a stream of back-to-back calls over
+    distinct input copies (`_stream_per_call`)."""
     import torch
     import nf4_weight_quantized_quantize_gb300 as nf4
 
@@ -686,10 +690,19 @@ def configs_block(dev, reps: int = 50):
             e = {"ms": t, "TFLOP/s": tf, "GB/s": gbs, "bytes": byts}
             if m >= 128:
                 e["frac_bf16"] = tf / pk["bf16_tflops"]
+                if cfg.m >= 2048:
+                    ms_s, copies, ncalls = _stream_per_call(x, p, a, cfg.n, y, wsp, stream, calls=32, copy_x=True)
+                    tf_s = 2 * m * cfg.n * cfg.k / (ms_s * 1e-3) / 1e12
+                    e["stream"] = {"ms_per_call": ms_s, "TFLOP/s": tf_s, "frac_bf16": tf_s / pk["bf16_tflops"],
+                                   "input_copies": copies, "calls": ncalls,
+                                   "how": "back-to-back calls over distinct weight and activation copies (> 3x "
+                                          "L2 in all), replayed as one CUDA graph between one pair of events: "
+                                          "the per-call time of layers run one after another, without the "
+                                          "launch latency a lone call between events pays"}
             else:
                 e["frac_hbm"] = gbs / pk["hbm_gbs"]
                 if numel * 0.5625 >= 4e6:   # a weight L2 cannot hold three times over in a few copies
-                    ms_s, copies, ncalls = _skinny_stream(x, p, a, cfg.n, y, wsp, stream)
+                    ms_s, copies, ncalls = _stream_per_call(x, p, a, cfg.n, y, wsp, stream)
                     g_s = byts / (ms_s * 1e-3) / 1e9
                     e["stream"] = {"ms_per_call": ms_s, "GB/s": g_s, "frac_hbm": g_s / pk["hbm_gbs"],
                                    "weight_copies": copies, "calls": ncalls,
