@@ -59,7 +59,7 @@ __device__ __forceinline__ uint32_t quantize8(uint4 v, uint32_t am_bits, const f
 // a few ulps -- the fp32 sum 16 q + (16 + 1.5 * 2^23) rounds once, to the
 // integer c in the low mantissa bits (16 q is exact).  Cells are 1/16 wide
 // and neighbouring thresholds at least 0.08 apart, so the threshold T_k
-// nearest a cell's centre is the only one within 0.02 of any q in the cell,
+// nearest a cell's centre is the only one within 0.014 of any q in the cell,
 // and T_(k-1) < q < T_(k+1) there: the code of q is k + (q > T_k).  Entry c
 // is T_k with its low four fraction bits replaced by k + 1 (T_k moves by less
 // than 16 ulp, at most 2^-20).  So code = (bits(e) & 15) - 1 + (q > e), the

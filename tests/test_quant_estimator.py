@@ -129,3 +129,19 @@ def test_cell_entries_carry_their_threshold():
         ks.append(k)
     assert ks == sorted(ks) and ks[0] == 0 and ks[-1] == 14
     assert all(c == cells[32] for c in cells[33:])
+
+
+def test_cell_threshold_is_the_only_one_near_its_cell():
+    """Cell c covers q in [(c - 16.5) / 16, (c - 15.5) / 16]; its entry's
+    threshold T_k is the only threshold within 0.014 of that range, and
+    T_(k-1) < q < T_(k+1) on it -- the two facts the code rule rests on."""
+    _, _, cells = kernel_constants()
+    t = np.array(thresholds(), dtype=np.float64)
+    for c in range(33):
+        k = (cells[c] & 15) - 1
+        lo, hi = max(-1.0, (c - 16.5) / 16), min(1.0, (c - 15.5) / 16)
+        assert k == 0 or t[k - 1] < lo
+        assert k == 14 or t[k + 1] > hi
+        for j in range(15):
+            if j != k:
+                assert not (lo - 0.014 <= t[j] <= hi + 0.014), (c, j)
