@@ -11,6 +11,19 @@ namespace nf4 {
 constexpr int kBK = 64;                    // K per slice = one NF4 block = one 128-byte activation row
 constexpr int kPackedRow = kBK / 2;        // 32 packed bytes per weight row per slice
 
+// fp32 weights: one packed word (bytes in address order, code 2j in the high
+// nibble of byte j) to eight values C[code] * absmax in fp32 -- the fp32
+// dequantizer's values -- rounded to tf32, the part the MMA reads.  `code`
+// is the fp32 codebook in shared memory.
+__device__ __forceinline__ void expand8_f32(uint32_t p, const float* code, float am, uint32_t* o) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = (p >> (8 * j)) & 0xffu;
+        o[2 * j] = to_tf32(code[b >> 4] * am);
+        o[2 * j + 1] = to_tf32(code[b & 15u] * am);
+    }
+}
+
 // pfull[p] completes on the TMA bytes plus kPfullArrivals arrivals: the
 // weight producer lane's expect-tx arrive and one cp.async arrive per lane.
 constexpr int kPfullArrivals = 1 + 32;

@@ -209,18 +209,6 @@ struct TsArgs {
     uint32_t* err;
 };
 
-// fp32 weights: one packed word (bytes in address order, code 2j in the high
-// nibble of byte j) to eight values C[code] * absmax in fp32 -- the fp32
-// dequantizer's values -- rounded to tf32, the part the MMA reads.
-__device__ __forceinline__ void expand8_f32(uint32_t p, const float* code, float am, uint32_t* o) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t b = (p >> (8 * j)) & 0xffu;
-        o[2 * j] = to_tf32(code[b >> 4] * am);
-        o[2 * j + 1] = to_tf32(code[b & 15u] * am);
-    }
-}
-
 // DT: the compute dtype of X, Y and the converted weights: bf16 or fp16
 // (kind::f16) or fp32 (kind::tf32).
 template <int NX, int KS, int RS, int LUT, bool SPLIT, bool GEGLU, int DT>

@@ -1,7 +1,7 @@
 // nf4_gemm_wide.cu -- the fused NF4 GEMM for larger batches on CTA pairs:
-// Y[M, N] = X[M, K] . deq(W)[N, K]^T at bf16 or fp16, fp32 accumulation in
-// TMEM, tcgen05 kind::f16 with cta_group::2 (one MMA spans the tensor cores
-// of the two SMs of a CTA pair).
+// Y[M, N] = X[M, K] . deq(W)[N, K]^T at bf16, fp16 or fp32, fp32 accumulation
+// in TMEM, tcgen05 kind::f16 (kind::tf32 for fp32) with cta_group::2 (one MMA
+// spans the tensor cores of the two SMs of a CTA pair).
 //
 // This is the forward of the NF4 linear module of the diffuseR page "Gemma3
 // NF4 on GPU" (#39, Summary: ltx23_nf4_linear) for the prompt batches of the
@@ -24,10 +24,12 @@
 // A gate/up pair (GEGLU) takes 64 gate rows and the 64 up rows of the same
 // outputs per CTA and writes gelu_tanh(gate) * up.
 //
-// Rings (per CTA): activations, SX slots of one K-slice (NX rows x 128 bytes:
-// the CTA's halves of both accumulators, TMA with the 128-byte swizzle);
-// expanded weights, SA slots of one K-slice written by the converters;
-// packed weights, SP slots of two K-slices of packed bytes and fp32 scales.
+// Rings (per CTA): activations, SX slots of one ring slice (NX rows x 128
+// bytes: the CTA's halves of both accumulators, TMA with the 128-byte
+// swizzle); expanded weights, SA slots of one ring slice written by the
+// converters; packed weights, SP slots of two K-slices of packed bytes and
+// fp32 scales.  A ring slice is one K-slice (NF4 block) of a 16-bit type and
+// half of one of fp32 -- 128 bytes of each row either way.
 // Warps: 0 loads activations (both CTAs' copies complete on the even CTA's
 // barrier); 1 allocates TMEM (both CTAs) and in the even CTA issues the first
 // accumulator's MMAs; 2-17 are converters (both CTAs' arrive on the even
@@ -201,15 +203,34 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 
 // D (+)= A . B^T over the pair: A's rows split between the two CTAs (128
 // each, at the same shared-memory offset), B's columns likewise, D of each
-// SM in its own TMEM at the same address.
+// SM in its own TMEM at the same address.  kind::f16 for bf16 / fp16
+// operands, kind::tf32 for fp32 ones (read as tf32).
+template <int DT>
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (DT == kF32)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// The instruction descriptor of the pair's M = 256, N = NX MMAs.
+template <int DT, int NX>
+__host__ __device__ constexpr uint32_t wd_idesc() {
+    if constexpr (DT == kF32)
+        return idesc_tf32_f32(256, NX);
+    else
+        return idesc_f16kind_f32<DT>(256, NX);
 }
 
 // Arrive once on the barrier at this offset in both CTAs of the pair when
@@ -229,8 +250,12 @@ template <int NX, int DT, bool GEGLU>
 __global__ void __launch_bounds__(kWdThreads, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, const WdArgs args) {
     using C = WdCfg<NX>;
-    static_assert(DT == kBF16 || DT == kF16, "kind::f16 operand types");
+    static_assert(DT == kBF16 || DT == kF16 || DT == kF32, "compute dtypes");
     constexpr int SX = C::SX, SA = C::SA, SP = C::SP;
+    // A ring slice is 128 bytes of each row: one NF4 block (K-slice) of a
+    // 16-bit type, half of one of fp32 (read by the MMAs as tf32).
+    constexpr int SPB = DT == kF32 ? 2 : 1;                // ring slices per K-slice
+    constexpr int kSliceVals = 128 / elem_bytes<DT>();     // values of a row in one ring slice
     constexpr int HX = NX / 2;   // activation rows of one accumulator held by each CTA
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KB aligned
@@ -258,6 +283,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     constexpr int kRowsOut = GEGLU ? C::BW / 2 : C::BW;
     const int n0 = (pair / args.m_tiles) * (2 * kRowsOut) + static_cast<int>(rank) * kRowsOut;
     const int nk = args.K / kBK;
+    const int nks = nk * SPB;   // ring slices
     const int nst = (nk + kWdKs - 1) / kWdKs;
 
     if (threadIdx.x == 0) {
@@ -268,7 +294,9 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             mbar_init(xempty(i), kWdIssuers);
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(afull(i), kWdConvWarps);   // (even CTA) the 8 warps per CTA that expand a K-slice
+            // (even CTA) the warps of both CTAs that expand a ring slice: 8
+            // per CTA for a 16-bit type, 4 for fp32
+            mbar_init(afull(i), kWdConvWarps / SPB);
             mbar_init(aempty(i), kWdIssuers);
         }
         for (int i = 0; i < SP; ++i) {
@@ -279,6 +307,12 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         mbar_init(drain, kWdIssuers);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    const float* code_f32 = nullptr;   // fp32: the codebook, read by the converters
+    if constexpr (DT == kF32) {
+        __shared__ float s_code[16];
+        if (threadIdx.x < 16) s_code[threadIdx.x] = c_code[threadIdx.x];
+        code_f32 = s_code;
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_x);
@@ -297,14 +331,14 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     pdl_launch_dependents();
 
     if (warp == 0) {
-        // ---------------- activation producer: K-slice k into slot k % SX once
+        // ---------------- activation producer: ring slice k into slot k % SX once
         // the pair's MMAs that read its previous contents completed.  Both
         // CTAs' copies complete on the even CTA's xfull barrier, which the even
         // CTA arms with the pair's bytes (the odd CTA's may land first: the
         // barrier's transaction count goes below zero until it is armed).
         if (lane == 0) {
             int issued = 0;
-            for (int k = 0; k < nk; ++k) {
+            for (int k = 0; k < nks; ++k) {
                 const int x = k % SX;
                 if (k >= SX &&
                     !mbar_wait_cluster(xempty(x), ((k / SX) - 1) & 1, args.err, abort_flag, kErrTimeoutEmpty))
@@ -315,11 +349,11 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 const int r0 = m0 + static_cast<int>(rank) * HX;
                 if (rank == 0) {
                     mbar_arrive_expect_tx(xfull(x), 2 * C::XS);
-                    tma_load_2d(dst, &tm_x, xfull(x), k * kBK, r0);
-                    tma_load_2d(dst + HX * 128, &tm_x, xfull(x), k * kBK, r0 + NX);
+                    tma_load_2d(dst, &tm_x, xfull(x), k * kSliceVals, r0);
+                    tma_load_2d(dst + HX * 128, &tm_x, xfull(x), k * kSliceVals, r0 + NX);
                 } else {
-                    tma_load_2d_pair_leader(dst, &tm_x, xfull(x), k * kBK, r0);
-                    tma_load_2d_pair_leader(dst + HX * 128, &tm_x, xfull(x), k * kBK, r0 + NX);
+                    tma_load_2d_pair_leader(dst, &tm_x, xfull(x), k * kSliceVals, r0);
+                    tma_load_2d_pair_leader(dst + HX * 128, &tm_x, xfull(x), k * kSliceVals, r0 + NX);
                 }
                 ++issued;
             }
@@ -358,9 +392,11 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             // K-slice each waits until both CTAs expanded its weights and both
             // CTAs' activation halves landed, issues its 4 k-steps and commits
             // to both CTAs' barriers that release the K-slice's activation and
-            // expanded-weight slots (each counts both issuers' commits).
+            // expanded-weight slots (each counts both issuers' commits).  For
+            // fp32 the same per ring slice (half a K-slice, 4 tf32 k-steps of
+            // 8 values: 32 bytes of each row, as for a 16-bit type).
             const int acc = warp == 1 ? 0 : 1;
-            constexpr uint32_t idesc = idesc_f16kind_f32<DT>(256, NX);
+            constexpr uint32_t idesc = wd_idesc<DT, NX>();
             // descriptors of slot 0, k-step 0; a slot or a k-step adds to the
             // 14-bit start-address field (address / 16), which never carries:
             // shared-memory addresses stay below 2^18
@@ -368,7 +404,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem) + acc * HX * 128);
             const uint32_t d_tmem = tmem + acc * kWdAccStride;
             bool ok = true;
-            for (int k = 0; k < nk; ++k) {
+            for (int k = 0; k < nks; ++k) {
                 const int a = k % SA;
                 const int x = k % SX;
                 ok = mbar_wait_cluster(afull(a), (k / SA) & 1, args.err, abort_flag, kErrTimeoutConverted) &&
@@ -379,7 +415,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((x * C::XS) >> 4);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)   // k-step j of the K-slice: 32 bytes of each row
-                    mma_pair(d_tmem, ad + 2 * j, bd + 2 * j, idesc, (k == 0 && j == 0) ? 0u : 1u);
+                    mma_pair<DT>(d_tmem, ad + 2 * j, bd + 2 * j, idesc, (k == 0 && j == 0) ? 0u : 1u);
                 mma_commit_pair(xempty(x));
                 mma_commit_pair(aempty(a));
             }
@@ -399,7 +435,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int part = u / kWdKs;
         const int q = warp & 3;
         const int r = q * 32 + lane;   // weight row within this CTA's 128
-        const CodebookRegs cb = codebook_regs<DT>();
+        const CodebookRegs cb = codebook_regs<DT == kF32 ? kBF16 : DT>();   // (unused for fp32)
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         bool ok = true;
         for (int st = 0; st < nst; ++st) {
@@ -421,15 +457,30 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(pempty(p));   // this warp is done with packed slot p
             if (!live) continue;                      // the last stage of an odd number of K-slices
-            // the expanded slot must be free: the pair's MMAs of K-slice k - SA completed
-            const int a = k % SA;
-            const bool free_slot = k < SA || mbar_wait_cluster(aempty(a), ((k / SA) - 1) & 1, args.err,
+            // ring slice s: K-slice k, or (fp32) its half `part`; the expanded
+            // slot must be free: the pair's MMAs of ring slice s - SA completed
+            const int s = SPB * k + (SPB == 2 ? part : 0);
+            const int a = s % SA;
+            const bool free_slot = s < SA || mbar_wait_cluster(aempty(a), ((s / SA) - 1) & 1, args.err,
                                                                abort_flag, kErrTimeoutEmpty);
             if (!__all_sync(0xffffffffu, free_slot)) {
                 ok = false;
                 break;
             }
-            {
+            if constexpr (DT == kF32) {
+                // 32 values of row r (this half of the K-slice) in fp32, rounded
+                // to tf32: the whole 128-byte row of the slot, chunk c (4
+                // values) stored at chunk c ^ (r % 8)
+                uint32_t v[32];
+                expand8_f32(w4.x, code_f32, am, v + 0);
+                expand8_f32(w4.y, code_f32, am, v + 8);
+                expand8_f32(w4.z, code_f32, am, v + 16);
+                expand8_f32(w4.w, code_f32, am, v + 24);
+                const uint32_t row = a_base + a * C::A_KS + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    sts128(row + ((c ^ (r & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            } else {
                 // An absmax that is a DT value scales in one paired DT multiply
                 // (exact product, one rounding); any other absmax scales each
                 // value in fp32 and rounds once -- the dequantizer's value.
@@ -580,11 +631,15 @@ cudaError_t launch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, int
     if (cudaError_t e = set_smem(reinterpret_cast<const void*>(kernel), C::SMEM, dev.ordinal); e != cudaSuccess)
         return e;
     CUtensorMap tm_x, tm_w;
-    const CUtensorMapDataType xdt = DT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // activations: boxes of one K-slice (64 values, 128 bytes: the swizzle
-    // span) x NX / 2 rows; packed weights: boxes of two K-slices x 128 rows
-    // (x 64 rows for a gate/up pair, one box of gate rows and one of up rows)
-    if (!make_map(&tm_x, x, xdt, 2, M, K, NX / 2, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    constexpr CUtensorMapDataType xdt = DT == kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : DT == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    constexpr int eb = elem_bytes<DT>();
+    // activations: boxes of one ring slice (128 bytes of a row, the swizzle
+    // span: 64 values of a 16-bit type, 32 of fp32) x NX / 2 rows; packed
+    // weights: boxes of two K-slices x 128 rows (x 64 rows for a gate/up pair,
+    // one box of gate rows and one of up rows)
+    if (!make_map(&tm_x, x, xdt, eb, M, K, NX / 2, 128 / eb, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_w, packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, GEGLU ? C::BW / 2 : C::BW,
                   kPackedRow * kWdKs, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
@@ -626,6 +681,9 @@ cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, i
 
 }  // namespace
 
+// The tile kernel's time per K-slice and wave at fp32 (tf32 MMAs), in clocks.
+constexpr double kTsSliceF32Clk = 1640.0;
+
 // Whether the pair kernel takes this call, by a shape-only estimate of both
 // kernels' time: waves of one CTA per SM times the time of a K-slice.  Measured
 // on GB300 at M = 2048 (bf16, L2 flushed): about 0.52 us (1000 clocks) per
@@ -634,15 +692,20 @@ cudaError_t dispatch_wd(const DeviceInfo& dev, const WdPlan& p, const void* x, i
 // rate -- its MMAs scale with nx, its converters and signalling do not, so
 // smaller nx is not taken below the tile kernel's.
 bool wide_applies(int dtype, int64_t M, int64_t N) {
-    if ((dtype != kBF16 && dtype != kF16) || M <= 256) return false;
+    if ((dtype != kBF16 && dtype != kF16 && dtype != kF32) || M <= 256) return false;
     const WdPlan p = make_wd_plan(M, N);
     if (p.nx < 160 || p.nx > 256) return false;
     constexpr double kSms = 152.0;
     const double n_tiles = std::ceil(N / 128.0);
     const double ts_waves = std::ceil(n_tiles * std::ceil(M / 256.0) / kSms);
     const double wd_waves = std::ceil(2.0 * p.n_pairs * p.m_tiles / kSms);
-    const double wd_slice = std::max(1000.0, 1060.0 * p.nx / 256.0);
-    return wd_waves * wd_slice < ts_waves * 1000.0;
+    double wd_slice = std::max(1000.0, 1060.0 * p.nx / 256.0);
+    double ts_slice = 1000.0;
+    if (dtype == kF32) {   // two ring slices per K-slice; the tile kernel's tf32 K-slice
+        wd_slice *= 2.0;
+        ts_slice = kTsSliceF32Clk;
+    }
+    return wd_waves * wd_slice < ts_waves * ts_slice;
 }
 
 cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, int64_t M, int64_t K,
@@ -657,6 +720,9 @@ cudaError_t launch_gemm_wide(const DeviceInfo& dev, int dtype, const void* x, in
         case kF16:
             return geglu ? dispatch_wd<kF16, true>(dev, p, x, M, K, packed, absmax, N, y, s)
                          : dispatch_wd<kF16, false>(dev, p, x, M, K, packed, absmax, N, y, s);
+        case kF32:
+            return geglu ? dispatch_wd<kF32, true>(dev, p, x, M, K, packed, absmax, N, y, s)
+                         : dispatch_wd<kF32, false>(dev, p, x, M, K, packed, absmax, N, y, s);
         default: return cudaErrorInvalidValue;
     }
 }

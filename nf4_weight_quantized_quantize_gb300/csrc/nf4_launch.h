@@ -84,7 +84,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int dtype, const void* x, int64_t
 
 // The CTA-pair NF4 GEMM (nf4_gemm_wide.cu): expanded weights in shared
 // memory, two TMEM accumulators, pair tiles of 256 weight rows x up to 512
-// activation rows (bf16 / fp16, M > 256).  wide_applies: whether it beats
+// activation rows (bf16 / fp16 / fp32, M > 256).  wide_applies: whether it beats
 // the tile kernel on this shape (a shape-only estimate; N = rows of the
 // weight); launch_gemm and launch_gemm_geglu use it then.  N: rows of the
 // weight; geglu: the weight is a gate/up pair (N = 2F) and Y is [M, F].

@@ -148,6 +148,7 @@ CASES = {
     "cta_pair": _linear_case(1500, 10000, 192, BF16),
     "cta_pair_f16_ragged": _linear_case(700, 30720, 128, F16),
     "cta_pair_gate_up": _linear_case(1500, 10000, 192, BF16, geglu=True),
+    "cta_pair_f32": _linear_case(1500, 10000, 192, F32),
     "noalloc_m16": _noalloc_case(16, 3840, 2048),
 }
 

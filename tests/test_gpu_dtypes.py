@@ -234,7 +234,10 @@ def linear_check(dtype, x_cpu, w_cpu, fn, n_cols, oracle_fn, rows=None):
 
 
 @pytest.mark.parametrize("M,N,K", [(2048, 4096, 3840), (16, 3840, 15360), (257, 300, 128), (130, 640, 1536),
-                                   (33, 1000, 64 * 50), (512, 256, 64)])
+                                   (33, 1000, 64 * 50), (512, 256, 64),
+                                   # CTA pairs at fp32 (two tf32 ring slices per K-slice): ragged M and
+                                   # N, an odd number of K-slices, nx = 256 and 192
+                                   (1500, 10000, 192), (2047, 4100, 320), (700, 30720, 128)])
 def test_linear_f32(M, N, K):
     """fp32 compute dtype: the tensor cores read tf32 (X's 10-bit fraction,
     the weight rounded to tf32), accumulate in fp32 and write fp32.  Per
@@ -259,6 +262,16 @@ def test_linear_geglu_f32(M):
     x = rand_w(M * K, 1.0, 191 + M, "f32").reshape(M, K)
     linear_check("f32", x, w, lambda xd, pd, ad: nf4.linear_geglu(xd, pd, ad, F), F,
                  lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f32"))
+
+
+@pytest.mark.parametrize("M,F,K", [(2048, 2432, 256), (1500, 2400, 320)])
+def test_linear_geglu_f32_pair_kernel(M, F, K):
+    """The fused gate/up pair at fp32 on CTA pairs (sampled rows)."""
+    w = rand_w(2 * F * K, 0.05, 290 + M, "f32").reshape(2 * F, K)
+    x = rand_w(M * K, 1.0, 291 + M, "f32").reshape(M, K)
+    rows = np.sort(np.random.default_rng(M + F).choice(M, 24, replace=False))
+    linear_check("f32", x, w, lambda xd, pd, ad: nf4.linear_geglu(xd, pd, ad, F), F,
+                 lambda xb, p, a: oracle.linear_geglu(xb, p, a, F, dtype="f32"), rows)
 
 
 def test_f32_close_to_bf16_on_shared_values():
