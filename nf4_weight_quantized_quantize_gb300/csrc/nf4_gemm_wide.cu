@@ -68,11 +68,11 @@ template <int NX>
 struct WdCfg {
     static constexpr int BW = 128;                             // weight rows per CTA
     static constexpr int XS = NX * 128;                        // activation slot: NX rows (2 halves of NX / 2)
-    static constexpr int A_KS = BW * 128;                      // one expanded K-slice (16 KB)
+    static constexpr int A_KS = BW * 128;                      // one expanded ring slice (16 KB)
     static constexpr int P_BYTES = BW * kPackedRow * kWdKs;    // packed bytes of a stage
     static constexpr int AM_BYTES = BW * 4 * kWdKs;            // scales of a stage
     static constexpr int P_SLOT = (P_BYTES + AM_BYTES + 1023) / 1024 * 1024;
-    static constexpr int SA = 4;                               // expanded-weight slots, one K-slice each
+    static constexpr int SA = 4;                               // expanded-weight slots, one ring slice each
     static constexpr int SP = 3;
     static constexpr int BUDGET = kWdSmemLimit - 1024 - 512;   // alignment slack; barriers and flags
     static constexpr int SX_FIT = (BUDGET - SA * A_KS - SP * P_SLOT) / XS;
@@ -414,7 +414,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 const uint64_t ad = a_desc0 + static_cast<uint64_t>((a * C::A_KS) >> 4);
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((x * C::XS) >> 4);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)   // k-step j of the K-slice: 32 bytes of each row
+                for (int j = 0; j < 4; ++j)   // k-step j of the ring slice: 32 bytes of each row
                     mma_pair<DT>(d_tmem, ad + 2 * j, bd + 2 * j, idesc, (k == 0 && j == 0) ? 0u : 1u);
                 mma_commit_pair(xempty(x));
                 mma_commit_pair(aempty(a));
