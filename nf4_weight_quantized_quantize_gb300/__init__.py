@@ -18,7 +18,9 @@ runs in the library's CUDA kernels:
   status.
 
 The library must have been built (``build.build()``); importing this package
-without it raises ImportError -- there is no fallback implementation.
+without it raises ImportError -- there is no fallback implementation.  The
+environment variable ``NF4_LIBRARY`` selects another build of it (for
+instance the bounds-checked one).
 """
 from __future__ import annotations
 
@@ -42,7 +44,10 @@ NF4_DTYPE_BF16 = 0
 NF4_DTYPE_F16 = 1
 NF4_DTYPE_F32 = 2
 BLOCK = 64
-LIB_PATH = _build.LIB
+# The environment variable NF4_LIBRARY names another build to load instead --
+# the bounds-checked one (``build.CHECKED_LIB``), to run a whole program or
+# test suite through it; unset, the in-tree libnf4.so.
+LIB_PATH = os.environ.get("NF4_LIBRARY") or _build.LIB
 
 
 def load_library(path: str) -> ctypes.CDLL:
@@ -78,7 +83,7 @@ def load_library(path: str) -> ctypes.CDLL:
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"libnf4.so is not built ({LIB_PATH}); run "
+            f"libnf4 is not built ({LIB_PATH}); run "
             "`python -m nf4_weight_quantized_quantize_gb300.build` first")
     return load_library(LIB_PATH)
 
