@@ -39,6 +39,8 @@ def faulty_lib():
     lib.nf4_linear.restype = ctypes.c_int
     lib.nf4_linear_geglu.argtypes = [P, I64, I64, P, P, I64, I32, P, P, SZ, P]
     lib.nf4_linear_geglu.restype = ctypes.c_int
+    lib.nf4_linear_ex.argtypes = [P, I32, I64, I64, P, P, I64, I32, P, P, SZ, P]
+    lib.nf4_linear_ex.restype = ctypes.c_int
     lib.nf4_last_error.argtypes = [P]
     lib.nf4_last_error.restype = ctypes.c_int
     return lib
@@ -84,6 +86,25 @@ def test_gate_up_pair_bounded_wait_expires(faulty_lib, m, f, k):
     stream = torch.cuda.current_stream().cuda_stream
     st = faulty_lib.nf4_linear_geglu(x.data_ptr(), m, k, pd.data_ptr(), ad.data_ptr(), f, 64, y.data_ptr(),
                                      None, 0, stream)
+    assert st == nf4.NF4_OK
+    assert faulty_lib.nf4_last_error(stream) == nf4.NF4_ERR_TIMEOUT
+    assert faulty_lib.nf4_last_error(stream) == nf4.NF4_OK
+
+
+def test_fp32_pair_bounded_wait_expires(faulty_lib):
+    """The CTA-pair kernel's fp32 form: two ring slices per K-slice, each
+    expanded by four converter warps per CTA; withholding the first stage's
+    reports leaves four slices incomplete and the issuers' waits run out."""
+    m, n, k = 1500, 10000, 192
+    rs = np.random.default_rng(11)
+    w = (rs.standard_normal((n, k)) * 0.02).astype(np.float32)
+    x = torch.from_numpy(rs.standard_normal((m, k)).astype(np.float32)).to(DEV)
+    p, a = oracle.quantize(w.reshape(-1), dtype="f32")
+    pd, ad = torch.from_numpy(p).to(DEV), torch.from_numpy(a).to(DEV)
+    y = torch.empty(m, n, dtype=torch.float32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = faulty_lib.nf4_linear_ex(x.data_ptr(), nf4.NF4_DTYPE_F32, m, k, pd.data_ptr(), ad.data_ptr(), n, 64,
+                                  y.data_ptr(), None, 0, stream)
     assert st == nf4.NF4_OK
     assert faulty_lib.nf4_last_error(stream) == nf4.NF4_ERR_TIMEOUT
     assert faulty_lib.nf4_last_error(stream) == nf4.NF4_OK
